@@ -1,0 +1,222 @@
+"""ctypes binding of ``libkda.so`` (the C ABI in ``include/kda.h``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  torch supplies device memory and the current stream.  There is no
+fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_CSRC = os.path.join(_PKG, "csrc")
+_INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
+_BUILD = os.path.join(_PKG, "_build")
+_LIB = os.path.join(_BUILD, "libkda.so")
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
+          3: "KDA_ERR_CUDA", 4: "KDA_ERR_OUT_OF_MEMORY", 5: "KDA_ERR_DEVICE_INPUT"}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def _sources():
+    return sorted(os.path.join(_CSRC, f) for f in os.listdir(_CSRC) if f.endswith(".cu"))
+
+
+def _headers():
+    hs = [os.path.join(_CSRC, f) for f in os.listdir(_CSRC) if f.endswith((".h", ".cuh"))]
+    return hs + [os.path.join(_INCLUDE, "kda.h")]
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every ``csrc/*.cu`` for sm_103a and link ``_build/libkda.so``.
+
+    Translation units compile in parallel; nvcc cross-compiles, so no GPU is
+    needed.  Rebuilds only when a source or header is newer than the library.
+    """
+    os.makedirs(_BUILD, exist_ok=True)
+    srcs = _sources()
+    newest = max(os.path.getmtime(p) for p in srcs + _headers())
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
+        return _LIB
+    common = ["nvcc", *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+              "-I", _INCLUDE, "-I", _CSRC, "--expt-relaxed-constexpr"]
+    objs, procs = [], []
+    for src in srcs:
+        obj = os.path.join(_BUILD, os.path.basename(src) + ".o")
+        objs.append(obj)
+        cmd = common + ["-c", src, "-o", obj]
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                             stderr=subprocess.STDOUT)))
+    failed = []
+    for cmd, p in procs:
+        out, _ = p.communicate()
+        if verbose or p.returncode:
+            print(out.decode(errors="replace"))
+        if p.returncode:
+            failed.append(" ".join(cmd))
+    if failed:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["nvcc", *ARCH_FLAGS, "-shared", "-o", tmp, *objs])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+def load():
+    """Load (building first if needed) the library; returns the ctypes handle."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _LIB if os.path.exists(_LIB) else build()
+            lib = ctypes.CDLL(path)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            lib.kda_chunk_fwd.restype = ctypes.c_int
+            lib.kda_chunk_fwd.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
+            lib.kda_chunk_fwd_split.restype = ctypes.c_int
+            lib.kda_chunk_fwd_split.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, i64, vp]
+            lib.kda_decode_step.restype = ctypes.c_int
+            lib.kda_decode_step.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
+            lib.kda_get_device_error.restype = ctypes.c_int
+            lib.kda_get_device_error.argtypes = [vp]
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_status_string.argtypes = [ctypes.c_int]
+            lib.kda_last_error_message.restype = ctypes.c_char_p
+            lib.kda_last_error_message.argtypes = []
+            lib.kda_abi_version.restype = ctypes.c_int
+            lib.kda_profile_enable.restype = None
+            lib.kda_profile_enable.argtypes = [ctypes.c_int]
+            lib.kda_profile_read.restype = ctypes.c_int
+            lib.kda_profile_read.argtypes = [ctypes.POINTER(_KernelTime), ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load().kda_last_error_message().decode(errors="replace")
+        raise KdaError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise KdaError(1, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise KdaError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise KdaError(1, f"{name} must be contiguous")
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, out=None,
+                  S_final=None, *, n_seqs=None, segment_tokens=0, want_state=True,
+                  stream=None):
+    """Prefill.  Tensors in the packed layout of ``include/kda.h``.
+
+    q, k: bf16 [T, H, dk] (or [B, T_b, H, dk], a uniform batch); v bf16;
+    log_alpha f32; beta f32 [T, H]; S0 f32 [N, H, dk, dv] or None;
+    cu_seqlens int32 [N+1] (CUDA) or None.  Returns (out, S_final).
+    """
+    if q.dim() == 4:  # uniform batch [B, T_b, H, d]
+        B = q.shape[0]
+        q, k, v = (x.reshape(-1, *x.shape[2:]) for x in (q, k, v))
+        log_alpha = log_alpha.reshape(-1, *log_alpha.shape[2:])
+        beta = beta.reshape(-1, beta.shape[-1])
+        if n_seqs is None:
+            n_seqs = B
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.shape[0] - 1
+    elif n_seqs is None:
+        n_seqs = 1
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S0, torch.float32, "S0"),
+                        (cu_seqlens, torch.int32, "cu_seqlens")):
+        _require(t, dt, name)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out")
+    _require(S_final, torch.float32, "S_final")
+    lib = load()
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+            _ptr(cu_seqlens), _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv]
+    if segment_tokens:
+        _check(lib.kda_chunk_fwd_split(*args, int(segment_tokens), _stream(stream)))
+    else:
+        _check(lib.kda_chunk_fwd(*args, _stream(stream)))
+    return out, S_final
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S_inout, out=None, *, stream=None):
+    """One decode step; ``S_inout`` [N, H, dk, dv] f32 is updated in place.
+
+    q, k: bf16 [N, H, dk]; v bf16 [N, H, dv]; log_alpha f32 [N, H, dk];
+    beta f32 [N, H].  Returns out bf16 [N, H, dv].
+    """
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S_inout, torch.float32, "S_inout")):
+        _require(t, dt, name)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out")
+    _check(load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                  _ptr(S_inout), _ptr(out), N, H, dk, dv, _stream(stream)))
+    return out
+
+
+def kda_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return load().kda_get_device_error(_stream(stream))
+
+
+def profile_enable(on: bool = True):
+    load().kda_profile_enable(1 if on else 0)
+
+
+def profile_read():
+    """{kernel name: (launches, total ms)} since the last read."""
+    buf = (_KernelTime * 32)()
+    n = load().kda_profile_read(buf, 32)
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(n)}

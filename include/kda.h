@@ -1,0 +1,192 @@
+/*
+ * kda.h -- C ABI of the Kimi Delta Attention (KDA) library for one GB300 GPU
+ * (sm_103a).
+ *
+ * The layer.  Per head, a state S of shape dk x dv (fp32) is carried along the
+ * sequence.  Token t with query q_t, key k_t (dk), value v_t (dv), per-channel
+ * log-decay log_alpha_t (dk) and write strength beta_t does
+ *
+ *     alpha_t = exp(clamp(log_alpha_t, -5, 0))                 (per key channel)
+ *     S_t     = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t     = S_t^T q_t                                        (updated state)
+ *
+ * Sources: lecture "Inside Kimi K3: Architecture of an Open Frontier Model",
+ * sequence paragraph (a fixed-size state rewritten by every token: diagonal
+ * forget gate first, then the beta-weighted k v correction; log-decay bounded
+ * below at -5); meridianbulletin.com article on Kimi K3, section "Handling One
+ * Million Tokens with a Fixed-Size State Matrix" (alpha kept in [e^-5, 1]).
+ * No 1/sqrt(dk) scale, output gate or normalisation is applied: a caller that
+ * wants one scales q or post-processes out.
+ *
+ * Conventions common to every entry point
+ * ----------------------------------------
+ * - All tensor pointers are DEVICE pointers of the current CUDA device, dense
+ *   row-major (innermost index last, no padding) and 16-byte aligned.
+ * - bf16 tensors are IEEE bfloat16; f32 tensors are IEEE binary32.
+ * - Supported head sizes: dk == dv, and dk in {64, 128}.  Anything else
+ *   returns KDA_ERR_UNSUPPORTED.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call is asynchronous with respect to the host and ordered
+ *   on `stream`; calls on different streams may run concurrently.
+ * - The caller owns every buffer.  The library keeps no caller pointer after
+ *   a call returns.  Inputs are never written.
+ * - Errors found on the host (null pointer, bad size, misalignment,
+ *   unsupported shape) are returned synchronously before anything is launched;
+ *   outputs are then untouched and kda_last_error_message() explains.
+ *   A failed launch or allocation returns KDA_ERR_CUDA / KDA_ERR_OUT_OF_MEMORY.
+ *   Errors only the GPU can see (a malformed cu_seqlens array) make the
+ *   kernels skip their work and raise a device error word, which
+ *   kda_get_device_error() reports.  No kernel traps or asserts.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, misaligned, ... */
+    KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. dk = 96)     */
+    KDA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed         */
+    KDA_ERR_OUT_OF_MEMORY = 4,    /* the stream-ordered workspace allocation failed */
+    KDA_ERR_DEVICE_INPUT = 5      /* the GPU rejected an input (bad cu_seqlens)   */
+} kda_status;
+
+/*
+ * kda_chunk_fwd -- chunk-parallel prefill.
+ *
+ * Evaluates the recurrence above for every token of every sequence and head,
+ * starting from S0, and writes every output o_t and each sequence's final
+ * state.  Tokens of a 64-token chunk are processed together and only the
+ * state is handed from chunk to chunk (meridianbulletin.com article, section
+ * "Parallelizing Sequential State Updates"); the cumulative decay inside a
+ * chunk is handled in 16-token tiles whose accumulated log-decay the clamp
+ * keeps within [-80, 0] (orkas.ai close read, section "A lower bound that
+ * deleted a GPU code path").  When there are too few (sequence, head) chains
+ * to fill the GPU, long sequences are split into segments whose zero-start
+ * state and transition are combined by a prefix scan (same section of the
+ * meridianbulletin.com article; orkas.ai close read, section "The bill comes
+ * due in the serving stack").  Results equal the token-by-token recurrence up
+ * to floating-point rounding.
+ *
+ * Tensors (T = total_tokens, N = n_seqs, H = n_heads):
+ *   q, k        bf16 [T, H, dk]       read
+ *   v           bf16 [T, H, dv]       read
+ *   log_alpha   f32  [T, H, dk]       read; clamped to [-5, 0] on load
+ *   beta        f32  [T, H]           read; expected in [0, 1]
+ *   S0          f32  [N, H, dk, dv]   read; NULL = zero initial state
+ *   cu_seqlens  i32  [N + 1]          read; NULL = N sequences of equal length
+ *                                     T / N (T must be divisible by N).
+ *                                     Otherwise cu_seqlens[0] = 0,
+ *                                     non-decreasing, cu_seqlens[N] = T;
+ *                                     sequence n owns tokens
+ *                                     cu_seqlens[n] .. cu_seqlens[n+1]-1.
+ *                                     Empty sequences are allowed (their
+ *                                     S_final is S0).  Checked on the GPU.
+ *   out         bf16 [T, H, dv]       written (every row)
+ *   S_final     f32  [N, H, dk, dv]   written; NULL = not produced.
+ *                                     May alias S0 exactly (in-place
+ *                                     continuation); no other overlap allowed.
+ * A uniform batch [B, T_b, H, d] is passed as T = B * T_b, N = B,
+ * cu_seqlens = NULL.  T = 0 or N = 0 is a valid no-op (S_final = S0).
+ *
+ * Memory: allocates a temporary workspace stream-ordered on `stream`
+ * (cudaMallocAsync / cudaFreeAsync) when sequences are split; size grows
+ * with (N + T / segment) * H * dk * (dv + dk) * 4 bytes.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *log_alpha, const float *beta,
+                         const float *S0, const int32_t *cu_seqlens, void *out,
+                         float *S_final, int64_t total_tokens, int32_t n_seqs,
+                         int32_t n_heads, int32_t dk, int32_t dv, void *stream);
+
+/*
+ * kda_chunk_fwd_split -- kda_chunk_fwd with an explicit segment length.
+ *
+ * segment_tokens = 0 chooses automatically (what kda_chunk_fwd does).
+ * segment_tokens > 0 must be a multiple of 64: every sequence longer than it
+ * is cut into segments of that many tokens (the last may be shorter), each
+ * segment's zero-start increment B and transition M are computed in
+ * parallel, the entry states S_in(j+1) = M_j S_in(j) + B_j are scanned, and
+ * the segments are replayed from their entry states.  segment_tokens < 0
+ * disables splitting.  The result is the same up to rounding; this is the
+ * scheduling knob behind the automatic choice.
+ */
+kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               void *out, float *S_final, int64_t total_tokens,
+                               int32_t n_seqs, int32_t n_heads, int32_t dk,
+                               int32_t dv, int64_t segment_tokens, void *stream);
+
+/*
+ * kda_decode_step -- one recurrent step for a batch of N sequences.
+ *
+ * Per (sequence n, head h): S' = Diag(alpha) S; a = S'^T k; b = S'^T q;
+ * u = beta (v - a); S = S' + k u^T (written back IN PLACE); o = S^T q
+ * = b + (q . k) u.  The cost per token is constant: one pass over the state
+ * (lecture "Inside Kimi K3...", sequence paragraph; orkas.ai close read,
+ * section "The bill comes due in the serving stack": the state is updated in
+ * place, so a step cannot be undone -- keep a copy to roll back).
+ *
+ * Tensors:
+ *   q, k       bf16 [N, H, dk]        read
+ *   v          bf16 [N, H, dv]        read
+ *   log_alpha  f32  [N, H, dk]        read; clamped to [-5, 0]
+ *   beta       f32  [N, H]            read
+ *   S_inout    f32  [N, H, dk, dv]    read and overwritten with the new state
+ *   out        bf16 [N, H, dv]        written
+ * out must not overlap any other argument.  N = 0 is a no-op.
+ * Allocates nothing.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta,
+                           float *S_inout, void *out, int32_t n_seqs,
+                           int32_t n_heads, int32_t dk, int32_t dv,
+                           void *stream);
+
+/*
+ * kda_get_device_error -- synchronise `stream`, then return and clear the
+ * device error word of the current device: KDA_OK, or KDA_ERR_DEVICE_INPUT
+ * when a kernel rejected an input (kda_last_error_message() names it), or
+ * KDA_ERR_CUDA when the synchronisation itself failed.
+ */
+kda_status kda_get_device_error(void *stream);
+
+/* Static description of a status code. */
+const char *kda_status_string(kda_status status);
+
+/* Detail of the last failure on the calling host thread ("" if none). */
+const char *kda_last_error_message(void);
+
+/* KDA_ABI_VERSION of the compiled library. */
+int kda_abi_version(void);
+
+/*
+ * Launch timing (tracing aid).  While enabled, every kernel the library
+ * launches is bracketed by CUDA events on its launch stream.
+ * kda_profile_read() synchronises the device, then reports per kernel name
+ * the launch count and the summed event time in milliseconds, and clears the
+ * record.  Returns the number of entries written (at most max_entries).
+ * Disabled by default; enabling costs two event records per launch.
+ */
+typedef struct {
+    char name[48];
+    int64_t launches;
+    double total_ms;
+} kda_kernel_time;
+
+void kda_profile_enable(int enable);
+int kda_profile_read(kda_kernel_time *entries, int max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */
