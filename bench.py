@@ -1,0 +1,480 @@
+"""Benchmark of the KDA library on one GB300 (or N replicas under torchrun).
+
+Default workload: batched prefill B4 H32 T4096 d128 (inputs larger than L2,
+resident in HBM).  One step = one kda_chunk_fwd call over the whole batch
+(every hot-path stage: decay scan, intra-chunk matrices, UT transform, state
+hand-off, segment split when chosen).  The batched decode workload (256
+sequences x 32 heads, d128, fresh inputs each step) is measured in the same
+run and reported under "decode".
+
+Prints one JSON line on rank 0.  `--impl reference` times the fp64 CPU
+oracle on the host cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+CHUNK = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3])
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def prefill_bytes(n_token_heads, n_seq_heads, d, has_s0):
+    """q, k, v (bf16), log_alpha (f32), beta (f32) read, out (bf16) written per
+    token-head; S0 read (if given) and S_final written per sequence-head."""
+    per_th = 3 * 2 * d + 4 * d + 4 + 2 * d
+    per_sh = 4 * d * d * (2 if has_s0 else 1)
+    return n_token_heads * per_th + n_seq_heads * per_sh
+
+
+def prefill_flops(n_token_heads, d, C=CHUNK):
+    """Fixed convention, triangular-aware: 6 d^2 (W S, Q S, K'^T U) plus
+    C(3 dk + 2 dv) for the intra-chunk products, per token-head."""
+    return n_token_heads * (6 * d * d + 5 * C * d)
+
+
+def decode_bytes(n_seq_heads, d):
+    """State read + write (f32) plus q, k, v, out (bf16), log_alpha (f32), beta."""
+    return n_seq_heads * (8 * d * d + 12 * d + 4)
+
+
+def decode_flops(n_seq_heads, d):
+    return n_seq_heads * 7 * d * d
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(path):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, src_file):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, or None
+    when absent or taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(ROOT, "gated_delta_rule_48_gb300", "csrc", src_file)
+    if not os.path.exists(src) or rec.get("source_sha") != source_sha(src):
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as fh:
+            rows = [r.strip().split(", ") for r in fh if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- ranks
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def _device_inputs(p):
+    cu = None if p.uniform else torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    return dict(q=p.q.cuda(), k=p.k.cuda(), v=p.v.cuda(), log_alpha=p.log_alpha.cuda(),
+                beta=p.beta.cuda(), S0=None if p.S0 is None else p.S0.cuda(), cu_seqlens=cu)
+
+
+def time_prefill(kb, p, steps, warmup, world):
+    """Device-resident inputs; K timed kda_chunk_fwd calls bracketed by a
+    barrier and a synchronize.  Returns (ms per step, per-kernel tracing)."""
+    d = _device_inputs(p)
+    out = torch.empty((p.total_T, p.H, p.dv), dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((p.n_seqs, p.H, p.dk, p.dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
+                         d["cu_seqlens"], out=out, S_final=S, n_seqs=p.n_seqs, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    if kb.kda_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    kb.profile_read()  # drop anything recorded so far
+    kb.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    kb.profile_enable(False)
+    kernels = kb.profile_read()
+    ms = start.elapsed_time(stop) / steps
+    return ms, kernels, clocks.summary()
+
+
+def time_prefill_e2e(kb, p, steps, warmup):
+    """Same calls through the public API from pinned HOST buffers: every step
+    copies that step's inputs host->device and reads out + S_final back."""
+    host = dict(q=p.q.pin_memory(), k=p.k.pin_memory(), v=p.v.pin_memory(),
+                log_alpha=p.log_alpha.pin_memory(), beta=p.beta.pin_memory(),
+                S0=None if p.S0 is None else p.S0.pin_memory())
+    dev = {k: (None if v is None else torch.empty_like(v, device="cuda"))
+           for k, v in host.items()}
+    cu = None if p.uniform else torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    out = torch.empty((p.total_T, p.H, p.dv), dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((p.n_seqs, p.H, p.dk, p.dv), dtype=torch.float32, device="cuda")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_h.numel() * out_h.element_size() + S_h.numel() * S_h.element_size()
+
+    def step():
+        for k, v in host.items():
+            if v is not None:
+                dev[k].copy_(v, non_blocking=True)
+        kb.kda_chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"],
+                         dev["S0"], cu, out=out, S_final=S, n_seqs=p.n_seqs, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / steps, h2d, d2h
+
+
+def time_decode(kb, dec, steps_per_run, warmup, runs=3):
+    """Batched decode: `steps_per_run` consecutive in-place steps with fresh
+    inputs per step (all resident on the device); the state (512 MiB for the
+    default workload) exceeds L2, so no flush is needed."""
+    q, k, v = dec.q.cuda(), dec.k.cuda(), dec.v.cuda()
+    la, b = dec.log_alpha.cuda(), dec.beta.cuda()
+    S = dec.S.cuda()
+    N, H, dk = dec.q.shape[1:4]
+    out = torch.empty((N, H, dec.v.shape[3]), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    n_in = q.shape[0]
+    for i in range(warmup):
+        kb.kda_decode_step(q[i % n_in], k[i % n_in], v[i % n_in], la[i % n_in], b[i % n_in],
+                           S, out, stream=stream)
+    torch.cuda.synchronize()
+    kb.profile_read()
+    kb.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(runs):
+        for i in range(steps_per_run):
+            j = i % n_in
+            kb.kda_decode_step(q[j], k[j], v[j], la[j], b[j], S, out, stream=stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    kb.profile_enable(False)
+    kernels = kb.profile_read()
+    return start.elapsed_time(stop) / (runs * steps_per_run), kernels
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_sample(p, n_seqs):
+    """The first `n_seqs` sequences of a workload (all heads)."""
+    from gated_delta_rule_48_gb300 import inputs as kin
+    t1 = int(p.cu_seqlens[n_seqs])
+    return dict(q=kin.bf16_bits(p.q[:t1]), k=kin.bf16_bits(p.k[:t1]), v=kin.bf16_bits(p.v[:t1]),
+                log_alpha=p.log_alpha[:t1].numpy(), beta=p.beta[:t1].numpy(),
+                S0=None if p.S0 is None else p.S0[:n_seqs].numpy(),
+                cu=p.cu_seqlens[:n_seqs + 1].copy(), tokens=t1)
+
+
+def time_oracle(sample, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward(sample["q"], sample["k"], sample["v"], sample["log_alpha"], sample["beta"],
+                   sample["S0"], sample["cu"], threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def workload_config(p, idx):
+    from gated_delta_rule_48_gb300 import inputs as kin
+    lens = np.diff(p.cu_seqlens)
+    return {"workload": kin.WORKLOADS[idx], "n_seqs": p.n_seqs, "heads": p.H, "dk": p.dk,
+            "dv": p.dv, "tokens": p.total_T, "seq_len": int(lens.max()) if lens.size else 0,
+            "chunk": CHUNK, "l2": "inputs larger than L2 (no flush)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    from gated_delta_rule_48_gb300 import inputs as kin
+    import oracle
+    if rank != 0:
+        return
+    oracle.build()
+    p = kin.workload(args.workload)
+    n = 1
+    sample = cpu_sample(p, n)
+    threads = oracle.default_threads()
+    for _ in range(min(args.warmup, 1)):
+        time_oracle(sample, threads)
+    per = [time_oracle(sample, threads) for _ in range(max(1, min(args.steps, 3)))]
+    sec = statistics.mean(per)
+    value = sample["tokens"] / sec / 1e6
+    desc = f"sequence 0 of the workload ({sample['tokens']} tokens x {p.H} heads), fp64"
+    line = {"impl": "reference", "metric": "KDA prefill throughput", "value": value,
+            "unit": "Mtok/s", "n_gpus": world, "steps": len(per), "warmup": min(args.warmup, 1),
+            "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(p, args.workload),
+            "cpu_baseline": {"value": value, "unit": "Mtok/s", "cores": threads,
+                             "kind": "oracle", "sample": desc, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": "Mtok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        barrier(world)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the library arm")
+
+    import gated_delta_rule_48_gb300 as kda
+    from gated_delta_rule_48_gb300 import binding as kb
+    from gated_delta_rule_48_gb300 import inputs as kin
+
+    kda.build()
+    peaks, peak_src = load_peaks()
+    p = kin.workload(args.workload)
+    d = p.dk
+    th = p.total_T * p.H
+    sh = p.n_seqs * p.H
+    alg_bytes = prefill_bytes(th, sh, d, p.S0 is not None)
+    alg_flops = prefill_flops(th, d)
+
+    ms, kernels, clocks = time_prefill(kb, p, args.steps, args.warmup, world)
+    ms = max_over_ranks(ms, world)
+    tokens_all = sum_over_ranks(p.total_T, world)
+    value = tokens_all / (ms * 1e-3) / 1e6  # Mtok/s over all ranks
+
+    # dominant kernel: the one with the largest summed time in the timed region
+    launches = sum(n for n, _ in kernels.values())
+    top_name, (top_n, top_ms) = max(kernels.items(), key=lambda kv: kv[1][1])
+    top_avg_ms = top_ms / top_n
+    # algorithmic bytes per launch: the replay launch covers the whole batch once
+    per_launch_bytes = alg_bytes * (args.steps / top_n)
+    achieved_gbs = per_launch_bytes / (top_avg_ms * 1e-3) / 1e9
+    tflops = alg_flops / (ms * 1e-3) / 1e12
+    traffic = recorded_traffic(top_name, "kda_prefill_simt.cu")
+
+    line = {
+        "metric": "KDA prefill throughput", "value": value, "unit": "Mtok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(p, args.workload),
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": traffic, "kernel": top_name, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": per_launch_bytes},
+        "tensor": {"tflops": tflops, "bf16_peak": peaks["bf16_tflops"],
+                   "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+                   "algorithmic_flops_per_step": alg_flops, "peak_source": peak_src},
+        "kernels": {k: {"launches": n, "avg_ms": t / n} for k, (n, t) in kernels.items()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_prefill_e2e(kb, p, max(3, min(args.steps, 20)), 2)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        line["e2e"] = {"value": tokens_all / (e2e_ms * 1e-3) / 1e6, "unit": "Mtok/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms}
+
+    if not args.no_decode:
+        dec = kin.decode_workload(steps=args.decode_steps)
+        n_sh = dec.q.shape[1] * dec.q.shape[2]
+        dms, dk_kernels = time_decode(kb, dec, args.decode_steps, args.warmup)
+        dbytes = decode_bytes(n_sh, dec.q.shape[3])
+        dn, dt = dk_kernels["kda_decode_step"]
+        kern_gbs = dbytes / (dt / dn * 1e-3) / 1e9
+        line["decode"] = {
+            "workload": kin.WORKLOADS[4], "value": dbytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": dms, "tokens_per_s": n_sh / dec.q.shape[2] / (dms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": kern_gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("kda_decode_step", "kda_decode.cu"),
+                         "kernel": "kda_decode_step", "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": dbytes}}
+        del dec
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.default_threads()
+        sample = cpu_sample(p, min(p.n_seqs, 4))
+        sec = time_oracle(sample, threads)
+        line["cpu_baseline"] = {
+            "value": sample["tokens"] / sec / 1e6, "unit": "Mtok/s", "cores": threads,
+            "kind": "oracle", "cpu": cpu_model(), "seconds": sec,
+            "sample": f"first {min(p.n_seqs, 4)} sequences of the workload ({sample['tokens']} "
+                      f"tokens x {p.H} heads), fp64 token-by-token recurrence"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,388 @@
+// Host side of the C ABI (include/kda.h): argument checks, per-device state,
+// the stream-ordered workspace, the prefill schedule and launch tracing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace kda {
+
+// Device error word: kernels OR DeviceError flags into it; never trap.
+__device__ int g_device_error = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+kda_status fail(kda_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+kda_status cuda_fail(cudaError_t e, const char* what) {
+  kda_status st = (e == cudaErrorMemoryAllocation) ? KDA_ERR_OUT_OF_MEMORY : KDA_ERR_CUDA;
+  return fail(st, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- per device
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int* err = nullptr;          // address of g_device_error on this device
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_dev_mu;
+std::vector<DeviceState> g_devs;
+
+kda_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if ((int)g_devs.size() <= dev) g_devs.resize(dev + 1);
+  DeviceState& d = g_devs[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&d.pool, &props);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = ~0ull;  // keep freed workspace cached in the pool
+    e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+    d.ready = true;
+  }
+  *out = &d;
+  return KDA_OK;
+}
+
+// ---------------------------------------------------------------- tracing
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof_open, g_prof_done;
+
+// ---------------------------------------------------------------- checks
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+struct Range {
+  const char* name;
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const char* name, const void* p, int64_t bytes) {
+  uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{name, lo, p ? lo + static_cast<uintptr_t>(bytes) : lo};
+}
+
+bool overlaps(const Range& a, const Range& b) {
+  if (a.lo == a.hi || b.lo == b.hi) return false;
+  return a.lo < b.hi && b.lo < a.hi;
+}
+
+kda_status check_head_dims(int32_t dk, int32_t dv) {
+  if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "dk=%d dv=%d must be positive", dk, dv);
+  if (dk != dv || (dk != 64 && dk != 128))
+    return fail(KDA_ERR_UNSUPPORTED, "only dk == dv in {64, 128} is supported (got dk=%d dv=%d)", dk, dv);
+  return KDA_OK;
+}
+
+}  // namespace
+
+void prof_begin(cudaStream_t s, const char* name) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  ProfRecord r{name, nullptr, nullptr};
+  if (cudaEventCreate(&r.start) != cudaSuccess) return;
+  if (cudaEventCreate(&r.stop) != cudaSuccess) { cudaEventDestroy(r.start); return; }
+  cudaEventRecord(r.start, s);
+  g_prof_open.push_back(r);
+}
+
+void prof_end(cudaStream_t s, const char* name) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  for (size_t i = g_prof_open.size(); i-- > 0;) {
+    if (g_prof_open[i].name == name) {
+      cudaEventRecord(g_prof_open[i].stop, s);
+      g_prof_done.push_back(g_prof_open[i]);
+      g_prof_open.erase(g_prof_open.begin() + i);
+      return;
+    }
+  }
+}
+
+// Segment length used when the caller asks for the automatic choice.
+// Splitting pays when the (sequence, head) chains alone cannot fill the GPU:
+// the summary pass costs about as much as the replay again, so split only
+// when fewer than half the SMs would be busy, and then aim at about two
+// replay units per SM.
+static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count) {
+  const int64_t chains = static_cast<int64_t>(N) * H;
+  if (T <= 0 || N <= 0) return -1;
+  if (chains * 2 >= sm_count) return -1;
+  const int64_t want_units = 2LL * sm_count;
+  const int64_t extra = want_units / H - N;  // segments beyond one per sequence
+  if (extra <= 0) return -1;
+  int64_t L = (T + extra - 1) / extra;
+  L = (L + kChunk - 1) / kChunk * kChunk;
+  L = std::max<int64_t>(L, 4 * kChunk);
+  return L;
+}
+
+static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* beta,
+                                 const float* S0, const int32_t* cu_seqlens, void* out,
+                                 float* S_final, int64_t T, int32_t N, int32_t H,
+                                 int32_t dk, int32_t dv, int64_t segment_tokens,
+                                 void* stream_v) {
+  // ---- host-side checks: nothing is launched unless all pass
+  if (T < 0 || N < 0 || H <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "total_tokens=%lld n_seqs=%d n_heads=%d",
+                (long long)T, N, H);
+  kda_status st = check_head_dims(dk, dv);
+  if (st != KDA_OK) return st;
+  if (N == 0 && T > 0) return fail(KDA_ERR_INVALID_ARGUMENT, "tokens given but n_seqs = 0");
+  if (!cu_seqlens && N > 0 && T % N != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "cu_seqlens is NULL but total_tokens=%lld is not a multiple of n_seqs=%d",
+                (long long)T, N);
+  if (segment_tokens > 0 && segment_tokens % kChunk != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "segment_tokens=%lld is not a multiple of %d",
+                (long long)segment_tokens, kChunk);
+  if (T > 0) {
+    const struct { const void* p; const char* n; } req[] = {
+        {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, "log_alpha"}, {beta, "beta"}, {out, "out"}};
+    for (auto& r : req)
+      if (!r.p) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", r.n);
+  }
+  const void* all[] = {q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final};
+  const char* names[] = {"q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"};
+  for (int i = 0; i < 9; ++i)
+    if (misaligned(all[i])) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
+  const int64_t qk_bytes = T * H * dk * 2, v_bytes = T * H * dv * 2;
+  const int64_t la_bytes = T * H * dk * 4, b_bytes = T * H * 4;
+  const int64_t s_bytes = static_cast<int64_t>(N) * H * dk * dv * 4;
+  Range in[] = {range_of("q", q, qk_bytes), range_of("k", k, qk_bytes), range_of("v", v, v_bytes),
+                range_of("log_alpha", log_alpha, la_bytes), range_of("beta", beta, b_bytes),
+                range_of("S0", S0, S0 ? s_bytes : 0),
+                range_of("cu_seqlens", cu_seqlens, cu_seqlens ? (N + 1) * 4 : 0)};
+  Range r_out = range_of("out", out, T > 0 ? v_bytes : 0);
+  Range r_sf = range_of("S_final", S_final, S_final ? s_bytes : 0);
+  for (int i = 0; i < 7; ++i) {
+    const Range& r = in[i];
+    if (overlaps(r_out, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps %s", r.name);
+    const bool exact_alias = (i == 5) && r.lo == r_sf.lo;  // S_final == S0 is allowed
+    if (!exact_alias && overlaps(r_sf, r))
+      return fail(KDA_ERR_INVALID_ARGUMENT, "S_final overlaps %s", r.name);
+  }
+  if (overlaps(r_out, r_sf)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps S_final");
+  if (N == 0) return KDA_OK;
+
+  // ---- device work
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != KDA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream_v);
+
+  int64_t L = segment_tokens;
+  if (L == 0) L = auto_segment_tokens(T, N, H, dev->sm_count);
+  bool split = L > 0 && L < T;
+  if (!split) L = -1;
+  const int64_t capacity64 = split ? static_cast<int64_t>(N) + (T + L - 1) / L + 1 : N;
+  if (capacity64 > (1LL << 30)) return fail(KDA_ERR_UNSUPPORTED, "too many segments");
+  const int32_t capacity = static_cast<int32_t>(capacity64);
+
+  // workspace: [segment count | segments | incr_trans | entry_state]
+  auto align_up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off_nseg = 0;
+  size_t off_segs = align_up(off_nseg + sizeof(int32_t));
+  size_t off_it = align_up(off_segs + sizeof(Segment) * capacity);
+  size_t it_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)(dv + dk) : 0;
+  size_t off_es = align_up(off_it + it_bytes);
+  size_t es_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)dv : 0;
+  size_t ws_bytes = align_up(off_es + es_bytes);
+
+  char* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+
+  PrefillArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.log_alpha = log_alpha;
+  a.beta = beta;
+  a.S0 = S0;
+  a.out = static_cast<uint16_t*>(out);
+  a.S_final = S_final;
+  a.T = T; a.N = N; a.H = H; a.dk = dk; a.dv = dv;
+  a.incr_trans = split ? reinterpret_cast<float*>(ws + off_it) : nullptr;
+  a.entry_state = split ? reinterpret_cast<float*>(ws + off_es) : nullptr;
+  a.plan.segs = reinterpret_cast<Segment*>(ws + off_segs);
+  a.plan.n_segs = reinterpret_cast<int32_t*>(ws + off_nseg);
+  a.plan.capacity = capacity;
+  a.err = dev->err;
+
+  kda_status result = KDA_OK;
+  e = launch_plan(cu_seqlens, T, N, L, a.plan, a.err, s);
+  if (e == cudaSuccess && split) e = launch_prefill_summary(a, s);
+  if (e == cudaSuccess && split) e = launch_segment_scan(a, s);
+  if (e == cudaSuccess) e = launch_prefill_replay(a, s);
+  if (e != cudaSuccess) result = cuda_fail(e, "prefill launch");
+  cudaError_t ef = cudaFreeAsync(ws, s);
+  if (result == KDA_OK && ef != cudaSuccess) result = cuda_fail(ef, "workspace free");
+  return result;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_chunk_fwd(const void* q, const void* k, const void* v,
+                                    const float* log_alpha, const float* beta,
+                                    const float* S0, const int32_t* cu_seqlens, void* out,
+                                    float* S_final, int64_t total_tokens, int32_t n_seqs,
+                                    int32_t n_heads, int32_t dk, int32_t dv, void* stream) {
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
+                        n_seqs, n_heads, dk, dv, 0, stream);
+}
+
+extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const void* v,
+                                          const float* log_alpha, const float* beta,
+                                          const float* S0, const int32_t* cu_seqlens,
+                                          void* out, float* S_final, int64_t total_tokens,
+                                          int32_t n_seqs, int32_t n_heads, int32_t dk,
+                                          int32_t dv, int64_t segment_tokens, void* stream) {
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
+                        n_seqs, n_heads, dk, dv, segment_tokens, stream);
+}
+
+extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* v,
+                                      const float* log_alpha, const float* beta,
+                                      float* S_inout, void* out, int32_t N, int32_t H,
+                                      int32_t dk, int32_t dv, void* stream) {
+  if (N < 0 || H <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs=%d n_heads=%d", N, H);
+  kda_status st = check_head_dims(dk, dv);
+  if (st != KDA_OK) return st;
+  if (N == 0) return KDA_OK;
+  const struct { const void* p; const char* n; } req[] = {
+      {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, "log_alpha"},
+      {beta, "beta"}, {S_inout, "S_inout"}, {out, "out"}};
+  for (auto& r : req) {
+    if (!r.p) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", r.n);
+    if (misaligned(r.p)) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", r.n);
+  }
+  const int64_t nh = static_cast<int64_t>(N) * H;
+  Range r_out = range_of("out", out, nh * dv * 2);
+  Range others[] = {range_of("q", q, nh * dk * 2), range_of("k", k, nh * dk * 2),
+                    range_of("v", v, nh * dv * 2), range_of("log_alpha", log_alpha, nh * dk * 4),
+                    range_of("beta", beta, nh * 4), range_of("S_inout", S_inout, nh * dk * dv * 4)};
+  for (auto& r : others)
+    if (overlaps(r_out, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps %s", r.name);
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(others[5], others[i]))
+      return fail(KDA_ERR_INVALID_ARGUMENT, "S_inout overlaps %s", others[i].name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+                                static_cast<const uint16_t*>(v), log_alpha, beta, S_inout,
+                                static_cast<uint16_t*>(out), N, H, dk, dv, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KDA_OK;
+}
+
+extern "C" kda_status kda_get_device_error(void* stream) {
+  DeviceState* dev = nullptr;
+  kda_status st = device_state(&dev);
+  if (st != KDA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, dev->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word == 0) return KDA_OK;
+  int zero = 0;
+  e = cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  std::string msg;
+  if (word & kDevErrCuSeqlens)
+    msg += "cu_seqlens is malformed (cu[0] != 0, decreasing, or cu[N] != total_tokens); ";
+  if (word & kDevErrCapacity) msg += "segment plan exceeded its workspace; ";
+  return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
+}
+
+extern "C" const char* kda_status_string(kda_status status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_OUT_OF_MEMORY: return "KDA_ERR_OUT_OF_MEMORY";
+    case KDA_ERR_DEVICE_INPUT: return "KDA_ERR_DEVICE_INPUT";
+  }
+  return "unknown kda_status";
+}
+
+extern "C" const char* kda_last_error_message(void) { return t_last_error.c_str(); }
+
+extern "C" int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+extern "C" void kda_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+}
+
+extern "C" int kda_profile_read(kda_kernel_time* entries, int max_entries) {
+  cudaDeviceSynchronize();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  std::vector<kda_kernel_time> acc;
+  for (auto& r : g_prof_done) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.start, r.stop);
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+    auto it = std::find_if(acc.begin(), acc.end(),
+                           [&](const kda_kernel_time& t) { return strcmp(t.name, r.name) == 0; });
+    if (it == acc.end()) {
+      kda_kernel_time t;
+      memset(&t, 0, sizeof t);
+      strncpy(t.name, r.name, sizeof(t.name) - 1);
+      acc.push_back(t);
+      it = acc.end() - 1;
+    }
+    it->launches += 1;
+    it->total_ms += ms;
+  }
+  g_prof_done.clear();
+  int n = 0;
+  for (auto& t : acc) {
+    if (n >= max_entries || !entries) break;
+    entries[n++] = t;
+  }
+  return n;
+}

@@ -1,0 +1,125 @@
+// Single-token recurrent decode step, state updated in place.
+//
+// Per (sequence, head), with S of shape D x D (fp32, row c = key channel):
+//   S' = Diag(alpha) S,  a = S'^T k,  b = S'^T q,  u = beta (v - a),
+//   S  = S' + k u^T  (written back),  o = S^T q = b + (q . k) u.
+// One token costs one read and one write of the state, whatever the context
+// length (lecture "Inside Kimi K3: Architecture of an Open Frontier Model",
+// sequence paragraph: constant cost per new token; orkas.ai close read,
+// section "The bill comes due in the serving stack": the state is updated in
+// place).
+//
+// Memory-bound: 8 D^2 bytes of state traffic per (sequence, head) against
+// ~7 D^2 flops.  One CTA per (sequence, head); each thread keeps D/8 rows x 4
+// columns of the state in registers, loaded with 128-bit streaming loads
+// issued before any other work, so the whole 64 KiB tile is in flight at once.
+// A warp reads whole 512-byte rows (D = 128), so every access is coalesced.
+#include <cuda_runtime.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+template <int D>
+struct DecodeCfg {
+  static constexpr int kColGroups = D / 4;                 // float4 columns
+  static constexpr int kThreads = D == 128 ? 256 : 128;
+  static constexpr int kRowGroups = kThreads / kColGroups;  // 8
+  static constexpr int kRowsPerThread = D / kRowGroups;     // 16 or 8
+};
+
+template <int D>
+__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
+decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+              const uint16_t* __restrict__ v, const float* __restrict__ log_alpha,
+              const float* __restrict__ beta, float* __restrict__ S,
+              uint16_t* __restrict__ out) {
+  using Cfg = DecodeCfg<D>;
+  constexpr int CG = Cfg::kColGroups, RG = Cfg::kRowGroups, RPT = Cfg::kRowsPerThread;
+  const int64_t unit = blockIdx.x;  // sequence * H + head
+  const int tid = threadIdx.x;
+  const int cg = tid % CG, rg = tid / CG;
+
+  __shared__ float s_k[D], s_q[D], s_alpha[D], s_u[D];
+  __shared__ __align__(16) float s_red_a[RG][D + 4];
+  __shared__ __align__(16) float s_red_b[RG][D + 4];
+  __shared__ float s_qk;
+
+  // state tile: rows rg*RPT .. rg*RPT+RPT-1, columns 4*cg .. 4*cg+3
+  float4* Sp = reinterpret_cast<float4*>(S + unit * D * D);
+  float4 st[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) st[i] = __ldcs(&Sp[(rg * RPT + i) * CG + cg]);
+
+  const int64_t vec = unit * D;
+  for (int c = tid; c < D; c += Cfg::kThreads) {
+    s_k[c] = bf16_to_f32(k[vec + c]);
+    s_q[c] = bf16_to_f32(q[vec + c]);
+    s_alpha[c] = expf(clamp_log_alpha(log_alpha[vec + c]));
+  }
+  __syncthreads();
+
+  if (tid < 32) {  // q . k
+    float p = 0.f;
+    for (int c = tid; c < D; c += 32) p += s_q[c] * s_k[c];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if (tid == 0) s_qk = p;
+  }
+
+  float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int row = rg * RPT + i;
+    const float al = s_alpha[row], kr = s_k[row], qr = s_q[row];
+    st[i].x *= al; st[i].y *= al; st[i].z *= al; st[i].w *= al;
+    a[0] += st[i].x * kr; a[1] += st[i].y * kr; a[2] += st[i].z * kr; a[3] += st[i].w * kr;
+    b[0] += st[i].x * qr; b[1] += st[i].y * qr; b[2] += st[i].z * qr; b[3] += st[i].w * qr;
+  }
+  *reinterpret_cast<float4*>(&s_red_a[rg][4 * cg]) = make_float4(a[0], a[1], a[2], a[3]);
+  *reinterpret_cast<float4*>(&s_red_b[rg][4 * cg]) = make_float4(b[0], b[1], b[2], b[3]);
+  __syncthreads();
+
+  const float bt = beta[unit];
+  for (int col = tid; col < D; col += Cfg::kThreads) {
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) { sa += s_red_a[r][col]; sb += s_red_b[r][col]; }
+    const float u = bt * (bf16_to_f32(v[vec + col]) - sa);
+    s_u[col] = u;
+    out[vec + col] = f32_to_bf16(sb + s_qk * u);
+  }
+  __syncthreads();
+
+  const float u0 = s_u[4 * cg], u1 = s_u[4 * cg + 1], u2 = s_u[4 * cg + 2], u3 = s_u[4 * cg + 3];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float kr = s_k[rg * RPT + i];
+    float4 w = st[i];
+    w.x += kr * u0; w.y += kr * u1; w.z += kr * u2; w.w += kr * u3;
+    __stcs(&Sp[(rg * RPT + i) * CG + cg], w);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const float* log_alpha, const float* beta, float* S, uint16_t* out,
+                          int32_t N, int32_t H, int32_t dk, int32_t dv, cudaStream_t s) {
+  (void)dv;  // dk == dv is checked by the caller
+  const int64_t units = static_cast<int64_t>(N) * H;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  prof_begin(s, "kda_decode_step");
+  if (dk == 128)
+    decode_kernel<128><<<static_cast<unsigned>(units), DecodeCfg<128>::kThreads, 0, s>>>(
+        q, k, v, log_alpha, beta, S, out);
+  else
+    decode_kernel<64><<<static_cast<unsigned>(units), DecodeCfg<64>::kThreads, 0, s>>>(
+        q, k, v, log_alpha, beta, S, out);
+  prof_end(s, "kda_decode_step");
+  return cudaGetLastError();
+}
+
+}  // namespace kda

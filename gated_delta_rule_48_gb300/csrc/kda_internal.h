@@ -1,0 +1,96 @@
+// Internal declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;      // tokens per chunk
+constexpr int kSubTile = 16;    // tokens per decay tile inside a chunk
+constexpr float kLogAlphaMin = -5.0f;
+
+// Device error codes (bit flags OR-ed into the device error word).
+enum DeviceError : int {
+  kDevErrNone = 0,
+  kDevErrCuSeqlens = 1,      // cu_seqlens malformed
+  kDevErrCapacity = 2,       // more segments than the workspace holds
+};
+
+// One segment of one sequence: tokens [t0, t1) (global indices).
+struct Segment {
+  int64_t t0, t1;
+  int32_t seq;     // sequence index
+  int32_t index;   // segment index within its sequence
+  int32_t count;   // number of segments of that sequence
+  int32_t first;   // global id of that sequence's first segment
+};
+
+// Output of the planner, in device memory.
+struct Plan {
+  Segment* segs;       // [capacity]
+  int32_t* n_segs;     // [1] number of valid segments
+  int32_t capacity;
+};
+
+// Problem description shared by the prefill kernels.
+struct PrefillArgs {
+  const uint16_t* q;       // bf16 [T, H, dk]
+  const uint16_t* k;
+  const uint16_t* v;       // bf16 [T, H, dv]
+  const float* log_alpha;  // f32 [T, H, dk]
+  const float* beta;       // f32 [T, H]
+  const float* S0;         // f32 [N, H, dk, dv] or null
+  uint16_t* out;           // bf16 [T, H, dv]
+  float* S_final;          // f32 [N, H, dk, dv] or null
+  int64_t T;
+  int32_t N, H, dk, dv;
+  // split workspace (null when sequences are not split)
+  float* incr_trans;       // [capacity, H, dk, dv + dk]: B_j | M_j of each segment
+  float* entry_state;      // [capacity, H, dk, dv]: S_in(j) for j >= 1
+  Plan plan;               // segment list in the workspace
+  int* err;                // device error word
+};
+
+// ---- launch-time tracing (kda_api.cu)
+void prof_begin(cudaStream_t s, const char* name);
+void prof_end(cudaStream_t s, const char* name);
+
+// ---- planner and scan (kda_plan.cu)
+cudaError_t launch_plan(const int32_t* cu_seqlens, int64_t T, int32_t N,
+                        int64_t segment_tokens, Plan plan, int* err,
+                        cudaStream_t s);
+cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
+
+// ---- chunked prefill (kda_prefill_*.cu)
+// pass 0: summary (B_j, M_j) of every non-final segment; pass 1: replay.
+cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
+
+// ---- decode (kda_decode.cu)
+cudaError_t launch_decode(const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const float* log_alpha,
+                          const float* beta, float* S, uint16_t* out,
+                          int32_t N, int32_t H, int32_t dk, int32_t dv,
+                          cudaStream_t s);
+
+// bf16 helpers usable from device code without cuda_bf16.h conversions.
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+// round to nearest even; NaN stays NaN
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return 0x7fc0;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ float clamp_log_alpha(float la) {
+  return fminf(fmaxf(la, kLogAlphaMin), 0.0f);
+}
+
+}  // namespace kda

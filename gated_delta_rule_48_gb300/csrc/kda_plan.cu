@@ -1,0 +1,195 @@
+// Prefill schedule on the device, and the segment scan.
+//
+// The planner turns cu_seqlens (read on the GPU, so the host never waits)
+// into a list of segments: each sequence is cut into pieces of
+// `segment_tokens` tokens (a multiple of the 64-token chunk, so chunk
+// boundaries stay aligned to the sequence start), or kept whole.
+//
+// Splitting follows the decomposition the pages describe for spreading one
+// long sequence over many processors (meridianbulletin.com article, section
+// "Parallelizing Sequential State Updates"; orkas.ai close read, section "The
+// bill comes due in the serving stack"): a segment maps its entry state
+// affinely, S_end = M S_in + B, where B is the segment run from a zero state
+// and M the segment's transition.  The summary pass computes (B_j, M_j) of
+// every segment but each sequence's last; the scan below chains them,
+// S_in(j+1) = M_j S_in(j) + B_j, and the replay pass restarts each segment
+// from its exact entry state.
+#include <cuda_runtime.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Plan plan,
+            int* err) {
+  __shared__ int s_bad;
+  __shared__ int32_t s_scan[kPlanThreads];
+  __shared__ int32_t s_base;
+  const int tid = threadIdx.x;
+  if (tid == 0) { s_bad = 0; s_base = 0; }
+  __syncthreads();
+
+  // 1. validate cu_seqlens
+  if (cu) {
+    if (tid == 0 && (cu[0] != 0 || static_cast<int64_t>(cu[N]) != T)) atomicOr(&s_bad, 1);
+    for (int n = tid; n < N; n += kPlanThreads)
+      if (cu[n + 1] < cu[n]) atomicOr(&s_bad, 1);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) { atomicOr(err, kDevErrCuSeqlens); *plan.n_segs = 0; }
+    return;
+  }
+  const int64_t uni = N > 0 ? T / N : 0;
+
+  // 2. segments per sequence, exclusive scan, emit
+  for (int base = 0; base < N; base += kPlanThreads) {
+    const int n = base + tid;
+    int64_t t0 = 0, len = 0;
+    int32_t cnt = 0;
+    if (n < N) {
+      t0 = cu ? cu[n] : uni * n;
+      len = cu ? static_cast<int64_t>(cu[n + 1]) - cu[n] : uni;
+      cnt = 1;
+      if (L > 0 && len > L) cnt = static_cast<int32_t>((len + L - 1) / L);
+    }
+    s_scan[tid] = cnt;
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {  // Hillis-Steele inclusive scan
+      int32_t add = tid >= off ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += add;
+      __syncthreads();
+    }
+    const int32_t first = s_base + s_scan[tid] - cnt;
+    if (n < N) {
+      for (int32_t j = 0; j < cnt; ++j) {
+        const int32_t id = first + j;
+        if (id >= plan.capacity) { atomicOr(&s_bad, 2); break; }
+        Segment sg;
+        sg.t0 = t0 + (L > 0 ? static_cast<int64_t>(j) * L : 0);
+        sg.t1 = (j + 1 == cnt) ? t0 + len : sg.t0 + L;
+        sg.seq = n;
+        sg.index = j;
+        sg.count = cnt;
+        sg.first = first;
+        plan.segs[id] = sg;
+      }
+    }
+    __syncthreads();
+    if (tid == kPlanThreads - 1) s_base += s_scan[tid];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if (s_bad) {
+      atomicOr(err, kDevErrCapacity);
+      *plan.n_segs = 0;
+    } else {
+      *plan.n_segs = s_base;
+    }
+  }
+}
+
+// Entry states of split sequences: one CTA per (sequence, head, column block
+// of kScanCols state columns).  Sequential over the sequence's segments.
+constexpr int kScanCols = 32;
+constexpr int kScanThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kScanThreads)
+segment_scan_kernel(PrefillArgs a) {
+  const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kScanCols;
+  const int32_t n_segs = *a.plan.n_segs;
+  // find this sequence's first segment (segments are ordered by sequence)
+  __shared__ int32_t s_first, s_count;
+  __shared__ float sS[D][kScanCols];
+  __shared__ float sM[32][D + 1];  // 32 rows of M_j at a time
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_first = -1;
+    s_count = 0;
+    // binary search over segments for seq == n, index == 0
+    int lo = 0, hi = n_segs;
+    while (lo < hi) {
+      int mid = (lo + hi) >> 1;
+      if (a.plan.segs[mid].seq < n) lo = mid + 1; else hi = mid;
+    }
+    if (lo < n_segs && a.plan.segs[lo].seq == n) {
+      s_first = lo;
+      s_count = a.plan.segs[lo].count;
+    }
+  }
+  __syncthreads();
+  if (s_first < 0 || s_count <= 1) return;
+  const int W = a.dv + D;  // width of the B | M record
+  for (int i = tid; i < D * kScanCols; i += kScanThreads) {
+    const int c = i / kScanCols, j = i % kScanCols;
+    sS[c][j] = a.S0 ? a.S0[((static_cast<int64_t>(n) * a.H + h) * D + c) * a.dv + col0 + j] : 0.f;
+  }
+  __syncthreads();
+  for (int sgi = 0; sgi + 1 < s_count; ++sgi) {
+    const int64_t seg = s_first + sgi;
+    const float* rec = a.incr_trans + (seg * a.H + h) * static_cast<int64_t>(D) * W;
+    // each thread owns outputs (c, j) with j = tid % 32, c = tid / 32 + 8 r
+    float acc[D / 8];
+#pragma unroll
+    for (int r = 0; r < D / 8; ++r) {
+      const int c = tid / kScanCols + 8 * r;
+      acc[r] = rec[static_cast<int64_t>(c) * W + col0 + (tid % kScanCols)];  // B_j
+    }
+    for (int m0 = 0; m0 < D; m0 += 32) {
+      // stage M_j[:, m0:m0+32] transposed as sM[m][c]
+      __syncthreads();
+      for (int i = tid; i < D * 32; i += kScanThreads) {
+        const int c = i / 32, m = i % 32;
+        sM[m][c] = rec[static_cast<int64_t>(c) * W + a.dv + m0 + m];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < D / 8; ++r) {
+        const int c = tid / kScanCols + 8 * r;
+        float s = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) s += sM[m][c] * sS[m0 + m][tid % kScanCols];
+        acc[r] += s;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < D / 8; ++r) {
+      const int c = tid / kScanCols + 8 * r;
+      sS[c][tid % kScanCols] = acc[r];
+      a.entry_state[((seg + 1) * a.H + h) * static_cast<int64_t>(D) * a.dv +
+                    static_cast<int64_t>(c) * a.dv + col0 + (tid % kScanCols)] = acc[r];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* cu_seqlens, int64_t T, int32_t N, int64_t L, Plan plan,
+                        int* err, cudaStream_t s) {
+  prof_begin(s, "kda_plan");
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(cu_seqlens, T, N, L, plan, err);
+  prof_end(s, "kda_plan");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s) {
+  dim3 grid(a.N, a.H, a.dv / kScanCols);
+  prof_begin(s, "kda_segment_scan");
+  if (a.dk == 128)
+    segment_scan_kernel<128><<<grid, kScanThreads, 0, s>>>(a);
+  else
+    segment_scan_kernel<64><<<grid, kScanThreads, 0, s>>>(a);
+  prof_end(s, "kda_segment_scan");
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,129 @@
+"""The C ABI on the host: the library builds for sm_103a, loads, exports every
+entry point include/kda.h declares, and rejects bad arguments synchronously
+before touching the GPU (these calls never reach a CUDA API, so they run
+without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_48_gb300 import binding as kb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kb.build()
+    return kb.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("kda_chunk_fwd", "kda_decode_step", "kda_get_device_error",
+                 "kda_status_string", "kda_last_error_message", "kda_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported by {kb.library_path()}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kda_abi_version() == 1
+    assert lib.kda_status_string(0) == b"KDA_OK"
+    assert lib.kda_status_string(5) == b"KDA_ERR_DEVICE_INPUT"
+
+
+# fake, 16-byte aligned, non-overlapping device addresses: validation rejects
+# the call before any pointer is used
+BASE = 1 << 40
+STEP = 1 << 32
+
+
+def P(i, off=0):
+    return ctypes.c_void_p(BASE + i * STEP + off)
+
+
+def prefill(lib, T=128, N=2, H=2, dk=64, dv=64, ptrs=None, seg=None, **over):
+    p = {n: P(i) for i, n in enumerate(
+        ["q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"])}
+    p["cu_seqlens"] = None
+    p.update(over)
+    args = [p[n] for n in ["q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out",
+                           "S_final"]] + [T, N, H, dk, dv]
+    if seg is not None:
+        return lib.kda_chunk_fwd_split(*args, seg, None)
+    return lib.kda_chunk_fwd(*args, None)
+
+
+def test_prefill_rejects_unsupported_head_sizes(lib):
+    assert prefill(lib, dk=96, dv=96) == UNSUPPORTED
+    assert prefill(lib, dk=128, dv=64) == UNSUPPORTED
+    assert b"dk" in lib.kda_last_error_message()
+    assert prefill(lib, dk=0, dv=0) == INVALID
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "log_alpha", "beta", "out"])
+def test_prefill_rejects_null_required_pointer(lib, name):
+    assert prefill(lib, **{name: None}) == INVALID
+    assert name.encode() in lib.kda_last_error_message()
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "log_alpha", "beta", "S0", "out", "S_final"])
+def test_prefill_rejects_misaligned_pointer(lib, name):
+    idx = ["q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"].index(name)
+    assert prefill(lib, **{name: P(idx, 8)}) == INVALID
+    assert b"aligned" in lib.kda_last_error_message()
+
+
+def test_prefill_rejects_bad_sizes(lib):
+    assert prefill(lib, T=-1) == INVALID
+    assert prefill(lib, N=0, T=10) == INVALID
+    assert prefill(lib, H=0) == INVALID
+    assert prefill(lib, T=129, N=2) == INVALID        # uniform batch must divide
+    assert prefill(lib, seg=100) == INVALID            # segment not a multiple of 64
+
+
+def test_prefill_rejects_overlaps(lib):
+    assert prefill(lib, out=P(0, 64)) == INVALID          # out inside q
+    assert b"out overlaps" in lib.kda_last_error_message()
+    assert prefill(lib, S_final=P(5, 16)) == INVALID      # partial overlap with S0
+    assert prefill(lib, S_final=P(2)) == INVALID          # S_final over v
+    assert prefill(lib, S_final=P(7, 16)) == INVALID      # S_final inside out
+
+
+def test_prefill_empty_batch_is_a_noop(lib):
+    assert prefill(lib, T=0, N=0) == OK
+
+
+def decode(lib, N=4, H=2, dk=64, dv=64, **over):
+    p = {n: P(i) for i, n in enumerate(["q", "k", "v", "log_alpha", "beta", "S", "out"])}
+    p.update(over)
+    return lib.kda_decode_step(p["q"], p["k"], p["v"], p["log_alpha"], p["beta"], p["S"],
+                               p["out"], N, H, dk, dv, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode(lib, dk=32, dv=32) == UNSUPPORTED
+    assert decode(lib, S=None) == INVALID
+    assert decode(lib, out=P(0, 4)) == INVALID            # misaligned
+    assert decode(lib, out=P(5, 256)) == INVALID          # out inside the state
+    assert decode(lib, S=P(0, 16)) == INVALID             # state overlaps q
+    assert decode(lib, N=-1) == INVALID
+    assert decode(lib, N=0) == OK
+
+
+def test_build_targets_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in kb.ARCH_FLAGS
