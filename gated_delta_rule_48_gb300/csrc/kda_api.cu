@@ -333,6 +333,7 @@ extern "C" kda_status kda_get_device_error(void* stream) {
   if (word & kDevErrCuSeqlens)
     msg += "cu_seqlens is malformed (cu[0] != 0, decreasing, or cu[N] != total_tokens); ";
   if (word & kDevErrCapacity) msg += "segment plan exceeded its workspace; ";
+  if (word & kDevErrTimeout) msg += "a prefill kernel timed out waiting for its tensor-core work; ";
   return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
 }
 

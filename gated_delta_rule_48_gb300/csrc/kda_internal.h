@@ -18,6 +18,7 @@ enum DeviceError : int {
   kDevErrNone = 0,
   kDevErrCuSeqlens = 1,      // cu_seqlens malformed
   kDevErrCapacity = 2,       // more segments than the workspace holds
+  kDevErrTimeout = 4,        // a kernel gave up waiting on its own async copies / MMAs
 };
 
 // One segment of one sequence: tokens [t0, t1) (global indices).
@@ -69,6 +70,9 @@ cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 // pass 0: summary (B_j, M_j) of every non-final segment; pass 1: replay.
 cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
+// tcgen05 kernels (dk = dv = 128), kda_prefill_tc.cu
+cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s);
 
 // ---- decode (kda_decode.cu)
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k,

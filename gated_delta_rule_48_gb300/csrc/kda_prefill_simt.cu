@@ -236,12 +236,12 @@ cudaError_t launch_simt(const PrefillArgs& a, cudaStream_t s, const char* name) 
 }  // namespace
 
 cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s) {
-  return a.dk == 128 ? launch_simt<128, 0>(a, s, "kda_prefill_summary")
+  return a.dk == 128 ? launch_prefill_summary_tc(a, s)
                      : launch_simt<64, 0>(a, s, "kda_prefill_summary");
 }
 
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s) {
-  return a.dk == 128 ? launch_simt<128, 1>(a, s, "kda_prefill_replay")
+  return a.dk == 128 ? launch_prefill_replay_tc(a, s)
                      : launch_simt<64, 1>(a, s, "kda_prefill_replay");
 }
 
