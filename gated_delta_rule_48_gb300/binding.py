@@ -98,6 +98,8 @@ def load():
             lib.kda_chunk_fwd.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
             lib.kda_chunk_fwd_split.restype = ctypes.c_int
             lib.kda_chunk_fwd_split.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, i64, vp]
+            lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+            lib.kda_chunk_fwd_noalloc.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
             lib.kda_decode_step.restype = ctypes.c_int
             lib.kda_decode_step.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int

@@ -112,6 +112,16 @@ kda_status check_head_dims(int32_t dk, int32_t dv) {
 
 }  // namespace
 
+// Error reporting and the device error word for the other translation units.
+kda_status report_error(kda_status st, const char* msg) { return fail(st, "%s", msg); }
+
+kda_status device_error_word(int** out) {
+  DeviceState* dev = nullptr;
+  kda_status st = device_state(&dev);
+  if (st == KDA_OK) *out = dev->err;
+  return st;
+}
+
 void prof_begin(cudaStream_t s, const char* name) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (!g_prof_on) return;

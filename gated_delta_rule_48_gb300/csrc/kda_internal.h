@@ -56,6 +56,10 @@ struct PrefillArgs {
   int* err;                // device error word
 };
 
+// ---- error reporting shared by the entry points (kda_api.cu)
+kda_status report_error(kda_status st, const char* msg);  // sets kda_last_error_message()
+kda_status device_error_word(int** out);                   // current device's error word
+
 // ---- launch-time tracing (kda_api.cu)
 void prof_begin(cudaStream_t s, const char* name);
 void prof_end(cudaStream_t s, const char* name);

@@ -126,6 +126,36 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
                                int32_t dv, int64_t segment_tokens, void *stream);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd without any device allocation.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory during a call: runtimes that hand all
+ * device memory to their own allocator at start-up, and callers that must
+ * not touch a memory pool or take allocator locks in the middle of a step.
+ * It computes the same result as kda_chunk_fwd (same arguments, layouts and
+ * error rules) but keeps its working data -- the per-sequence schedule -- in
+ * a fixed 256 KiB array inside the library's device memory, which every GPU
+ * that loads the library holds until the process exits.  It never splits
+ * long sequences across SMs, so with few (sequence, head) chains it can be
+ * slower than kda_chunk_fwd.
+ *
+ * Limit: n_seqs <= 8184; larger batches return KDA_ERR_UNSUPPORTED (use
+ * kda_chunk_fwd).  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the one array: calls that
+ * overlap on the GPU (different streams, or different host threads without
+ * ordering) race and may produce wrong results; order them on one stream.
+ * Each call rebuilds the schedule it needs, so nothing carries over from
+ * the previous call.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *log_alpha, const float *beta,
+                                 const float *S0, const int32_t *cu_seqlens,
+                                 void *out, float *S_final, int64_t total_tokens,
+                                 int32_t n_seqs, int32_t n_heads, int32_t dk,
+                                 int32_t dv, void *stream);
+
+/*
  * kda_decode_step -- one recurrent step for a batch of N sequences.
  *
  * Per (sequence n, head h): S' = Diag(alpha) S; a = S'^T k; b = S'^T q;
