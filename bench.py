@@ -417,7 +417,7 @@ def main():
     per_launch_bytes = alg_bytes * (args.steps / top_n)
     achieved_gbs = per_launch_bytes / (top_avg_ms * 1e-3) / 1e9
     tflops = alg_flops / (ms * 1e-3) / 1e12
-    traffic = recorded_traffic(top_name, "kda_prefill_simt.cu")
+    traffic = recorded_traffic(top_name, "kda_prefill_tc.cu")
 
     line = {
         "metric": "KDA prefill throughput", "value": value, "unit": "Mtok/s",

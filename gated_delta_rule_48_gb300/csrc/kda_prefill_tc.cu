@@ -10,10 +10,10 @@
 //   strip products (bf16):  A_qk[r,i] = sum_c q_rc k_ic e^{g_rc - g_ic}  (i <= r)
 //                           A_kk[r,i] = beta_r sum_c k_rc k_ic e^{g_rc - g_ic}  (i < r)
 //   UT transform (fp32):    T = (I + A_kk)^{-1} Diag(beta)
-//   WY products (tf32/bf16): W^T = (k e^g)^T T^T,   U~^T = V^T T^T
+//   WY products:            W^T = (k e^g)^T T^T (tf32),  U~^T = V^T T^T (bf16 hi + lo)
 //   hand-off (tf32):        U^T = U~^T - S^T W^T
 //                           O^T = S^T (q e^g)^T + U^T A_qk^T        -> out
-//                           S^T <- S^T Diag(e^{g_last}) + U^T (k e^{g_last - g})
+//                           S^T <- S^T Diag(e^{g_last}) + U^T K',  K' = k e^{g_last - g}
 //
 // Tokens of a chunk are processed together and only the state is handed on
 // (meridianbulletin.com article, section "Parallelizing Sequential State
@@ -30,22 +30,19 @@
 // Operand precision: strip products in bf16 (their error only perturbs T and
 // the output); T is fp32 and enters the tf32 MMA rounded to nearest, and the
 // bf16 MMA with V (exact in bf16) as a hi + lo pair of bf16; every operand on
-// the state path is tf32 rounded to nearest; accumulation is fp32.
+// the state path is tf32 rounded to nearest; accumulation is fp32.  tf32
+// operands are always laid out K-major: the key-side factors k e^g and K' are
+// written transposed, [key channel][token].
 //
-// Phases of one chunk (256 threads, one MMA-issuing thread):
-//   1 decay scan + operand build (registers -> swizzled SMEM)   all warps
-//   2 strip MMA -> TMEM                                          thread 0
-//   3 strip read-out, UT transform                               all warps
-// (tf32 operands are always laid out K-major: the key-side factors k e^g and
-// K' are written transposed, [key channel][token].)
-//   4 W^T, U~^T MMAs                                             thread 0
-//   5 -W and q e^g to SMEM                                       all warps
-//   6 U^T -= S^T W^T ; O^T = S^T (q e^g)^T                       thread 0
-//   7 S^T column decay, U^T rounding, K' to SMEM                 all warps
-//   8 O^T += U^T A_qk^T ; S^T += U^T K'                          thread 0
-//   9 O^T -> out                                                 all warps
-// Raw q, k, log_alpha of the next chunk stream in by TMA from phase 1 on,
-// v from phase 4 on.
+// Schedule of chunk n (512 threads; thread 0 issues MMAs and TMA copies):
+//   A  strip MMA (n)                     || read O^T (n-1) out of TMEM -> out
+//   B  strip read-out, UT transform (in place), T to SMEM
+//   C  W^T, U~^T MMAs (n)                || K' (n) to SMEM
+//   D  -W and q e^g to SMEM
+//   E  U^T -= S^T W^T ; O^T = S^T (q e^g)^T
+//   F  decay the columns of S^T, round U^T to tf32 (in TMEM)
+//   G  O^T += U^T A_qk^T ; S^T += U^T K' || decay scan + operands of chunk n+1
+// Raw q, k, log_alpha stream in by TMA one chunk ahead; v after step C.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -63,44 +60,47 @@ using namespace sm100;
 
 constexpr int D = 128;          // dk = dv
 constexpr int C = kChunk;       // 64
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map (fp32 columns; 128 lanes)
-constexpr uint32_t kColS = 0;     // S^T          128 columns
-constexpr uint32_t kColA = 128;   // strip products 96 columns
-constexpr uint32_t kColW = 256;   // W^T           64 columns (lane = key channel)
-constexpr uint32_t kColU = 320;   // U^T           64 columns (lane = value channel)
-constexpr uint32_t kColO = 384;   // O^T           64 columns
+constexpr uint32_t kColS = 0;     // S^T            128 columns
+constexpr uint32_t kColA = 128;   // strip products  96 columns
+constexpr uint32_t kColW = 256;   // W^T             64 columns (lane = key channel)
+constexpr uint32_t kColU = 320;   // U^T             64 columns (lane = value channel)
+constexpr uint32_t kColO = 384;   // O^T             64 columns
 
 // Shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t kRawQ = 0;                 // bf16 [64][128] sw128 (2 blocks)
 constexpr uint32_t kRawK = kRawQ + 16384;
 constexpr uint32_t kRawV = kRawK + 16384;
 constexpr uint32_t kRawL = kRawV + 16384;     // f32 [64][128] sw128 (4 blocks)
-constexpr uint32_t kR = kRawL + 32768;        // phase-dependent operand region
-//   phase 1-2: strip A operand bf16 [128][128] at R, strip B operand [96][128] at R+32768
-//   phase 3-4: A_qk tf32 [64][64] at R, T tf32 at R+16384, T_hi/T_lo bf16 at R+32768/+40960,
-//              A_kk scratch f32 [64][kLdA] at R+49152, T' scratch f32 at R+49152+kScr
-//   phase 5-8: A_qk at R, q e^g tf32 [64][128] at R+16384
-//   phase 9:   output tile bf16 [64][128] (plain rows) at R+16384
-constexpr uint32_t kLdA = 68;                 // padded row stride (floats) of the scratch matrices
-constexpr uint32_t kScr = C * kLdA * 4;       // 17408
-constexpr uint32_t kRBytes = 49152 + 2 * kScr;
-// k e^g (transposed, [128 c][64 t]) -> -W ([64 t][128 c]) -> K' (transposed), all tf32 K-major
-constexpr uint32_t kKG = kR + ((kRBytes + 1023) / 1024) * 1024;
-constexpr uint32_t kMisc = kKG + 32768;
-// misc (floats): warp totals [8][128], G0 [128], G1 [128], g_last [128], e^{g_last} [128],
-// e^{G1 - G0} [128], beta [64]
-constexpr uint32_t kTot = kMisc;
-constexpr uint32_t kG0 = kTot + 8 * 128 * 4;
+constexpr uint32_t kR = kRawL + 32768;        // phase-dependent operand region (72 KiB):
+//   operands: strip A bf16 [128][128] at +0, strip B bf16 [96][128] at +32768
+//   UT:       T tf32 [64][64] at +0, T_hi / T_lo bf16 [64][64] at +16384 / +24576,
+//             A_kk -> T' f32 [64][kLdA] at +32768
+//   hand-off: q e^g tf32 [64][128] at +0
+//   always:   A_qk tf32 [64][64] at +57344
+constexpr uint32_t kLdA = 68;                 // padded row stride (floats)
+constexpr uint32_t kRT = 0, kRTh = 16384, kRTl = 24576, kRAkk = 32768, kRQ = 0;
+constexpr uint32_t kRAqk = 57344;
+constexpr uint32_t kKG = kR + 73728;          // k e^g (transposed) -> -W  tf32
+constexpr uint32_t kKP = kKG + 32768;         // K' (transposed)            tf32
+constexpr uint32_t kMisc = kKP + 32768;
+// f32 warp totals [16][128] of the decay scan: live only in the first half of
+// the operand build, inside the (then unused) strip-B operand area of R
+constexpr uint32_t kTot = kR + 40960;
+constexpr uint32_t kG0 = kMisc;
 constexpr uint32_t kG1 = kG0 + 512;
 constexpr uint32_t kGl = kG1 + 512;
 constexpr uint32_t kEGl = kGl + 512;
-constexpr uint32_t kE10 = kEGl + 512;
-constexpr uint32_t kBeta = kE10 + 512;
-constexpr uint32_t kBars = kBeta + 256;       // 3 mbarriers + TMEM slot
+constexpr uint32_t kBeta = kEGl + 512;
+constexpr uint32_t kBars = kBeta + 256;       // 3 mbarriers, TMEM slot, abort flag
 constexpr uint32_t kSmemBytes = kBars + 64 + 1024;  // + alignment slack
+static_assert(kRAkk + C * kLdA * 4 <= kRAqk, "A_kk scratch overlaps A_qk");
+static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct TcMaps {
   CUtensorMap q, k, v, la;
@@ -108,111 +108,114 @@ struct TcMaps {
 
 enum : int { kModeSummary = 0, kModeReplay = 1 };
 
-// Read 4 consecutive f32 (channels 4l..4l+3) of row r from a sw128 f32 tile.
-__device__ __forceinline__ float4 ld_f32x4(const unsigned char* tile, int r, int l) {
-  return *reinterpret_cast<const float4*>(tile + sw128_offset(C, r, 16 * l));
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
-// Read 4 consecutive bf16 of row r (channels 4l..4l+3) from a sw128 bf16 tile.
-__device__ __forceinline__ uint2 ld_bf16x4(const unsigned char* tile, int r, int l) {
-  return *reinterpret_cast<const uint2*>(tile + sw128_offset(C, r, 8 * l));
-}
+
 __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
   f[0] = __uint_as_float(u.x << 16);
   f[1] = __uint_as_float(u.x & 0xffff0000u);
   f[2] = __uint_as_float(u.y << 16);
   f[3] = __uint_as_float(u.y & 0xffff0000u);
 }
-// Store 4 bf16 (channels 4l..) into row `row` of a sw128 bf16 tile with `rows` rows.
-__device__ __forceinline__ void st_bf16x4(unsigned char* tile, uint32_t rows, int row, int l,
-                                          const float (&f)[4]) {
-  uint2 u;
-  u.x = pack_bf16x2(f[0], f[1]);
-  u.y = pack_bf16x2(f[2], f[3]);
-  *reinterpret_cast<uint2*>(tile + sw128_offset(rows, row, 8 * l)) = u;
+__device__ __forceinline__ uint2 pack4_bf16(const float (&f)[4]) {
+  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
 }
-// Store 4 tf32 (channels 4l..) into row `row` of a sw128 32-bit tile with `rows` rows.
-__device__ __forceinline__ void st_tf32x4(unsigned char* tile, uint32_t rows, int row, int l,
-                                          const float (&f)[4]) {
-  uint4 u;
-  u.x = f32_to_tf32_rn(f[0]);
-  u.y = f32_to_tf32_rn(f[1]);
-  u.z = f32_to_tf32_rn(f[2]);
-  u.w = f32_to_tf32_rn(f[3]);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(rows, row, 16 * l)) = u;
+__device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
+  return make_uint4(f32_to_tf32_rn(f[0]), f32_to_tf32_rn(f[1]), f32_to_tf32_rn(f[2]),
+                    f32_to_tf32_rn(f[3]));
 }
 
-// T' = (I + A)^{-1} for a strictly lower-triangular 64 x 64 matrix A (fp32,
-// row stride kLdA).  The four 16 x 16 diagonal blocks are inverted by forward
-// substitution (one thread per column), then block rows are combined:
-// T'_ab = -T'_aa sum_{b <= c < a} A_ac T'_cb.  sT must be zero on entry.
-__device__ void unit_lower_inverse(const float* __restrict__ sA, float* __restrict__ sT, int tid) {
+// In place: sA holds a strictly lower-triangular 64 x 64 matrix A (f32, row
+// stride kLdA, zero on and above the diagonal); on return it holds
+// T' = (I + A)^{-1} (unit lower-triangular).  The four 16 x 16 diagonal
+// blocks are inverted by column-oriented forward substitution in registers
+// (one thread per column), then block rows are completed in order:
+// T'_ab = -T'_aa sum_{b <= c < a} A_ac T'_cb, with 2 x 2 register tiles.
+__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, int tid) {
+  float x[16];
   if (tid < 64) {
     const int b = tid >> 4, j = tid & 15;
     const float* Ab = sA + (16 * b) * kLdA + 16 * b;
-    float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      float s = 0.f;
+    for (int i = 0; i < 15; ++i) {
+      const float xi = x[i];
 #pragma unroll
-      for (int i = 0; i < r; ++i) s += Ab[r * kLdA + i] * x[i];
-      if (r > j) x[r] = -s;
+      for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * kLdA + i], xi, x[r]);
     }
-    float* Tb = sT + (16 * b) * kLdA + 16 * b;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const int b = tid >> 4, j = tid & 15;
+    float* Tb = sA + (16 * b) * kLdA + 16 * b;
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tb[r * kLdA + j] = x[r];
   }
   __syncthreads();
-  const int rr = tid >> 4, cc = tid & 15;
+  const int blk = tid >> 6, loc = tid & 63;
+  const int rr = 2 * (loc >> 3), cc = 2 * (loc & 7);
   for (int a = 1; a < 4; ++a) {
-    float xv[3] = {0.f, 0.f, 0.f};
-#pragma unroll
-    for (int b = 0; b < 3; ++b) {
-      if (b >= a) break;
-      float s = 0.f;
+    const bool active = blk < a;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      const int b = blk;
       for (int c = b; c < a; ++c) {
-        const float* Arow = sA + (16 * a + rr) * kLdA + 16 * c;
-        const float* Tcol = sT + (16 * c) * kLdA + 16 * b + cc;
+        const float* A0 = sA + (16 * a + rr) * kLdA + 16 * c;
+        const float* Tc = sA + (16 * c) * kLdA + 16 * b + cc;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s += Arow[i] * Tcol[i * kLdA];
+        for (int i = 0; i < 16; ++i) {
+          const float a0 = A0[i], a1 = A0[kLdA + i];
+          const float2 t = *reinterpret_cast<const float2*>(Tc + i * kLdA);
+          acc[0] = fmaf(a0, t.x, acc[0]);
+          acc[1] = fmaf(a0, t.y, acc[1]);
+          acc[2] = fmaf(a1, t.x, acc[2]);
+          acc[3] = fmaf(a1, t.y, acc[3]);
+        }
       }
-      xv[b] = s;
     }
     __syncthreads();
-#pragma unroll
-    for (int b = 0; b < 3; ++b)
-      if (b < a) sT[(16 * a + rr) * kLdA + 16 * b + cc] = xv[b];
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < 3; ++b) {
-      if (b >= a) break;
-      const float* Drow = sT + (16 * a + rr) * kLdA + 16 * a;
-      const float* Xcol = sT + (16 * a) * kLdA + 16 * b + cc;
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) s += Drow[i] * Xcol[i * kLdA];
-      xv[b] = -s;
+    float* Xab = sA + (16 * a + rr) * kLdA + 16 * blk + cc;
+    if (active) {
+      *reinterpret_cast<float2*>(Xab) = make_float2(acc[0], acc[1]);
+      *reinterpret_cast<float2*>(Xab + kLdA) = make_float2(acc[2], acc[3]);
     }
     __syncthreads();
+    if (active) {
+      const float* D0 = sA + (16 * a + rr) * kLdA + 16 * a;
+      const float* Xc = sA + (16 * a) * kLdA + 16 * blk + cc;
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
-    for (int b = 0; b < 3; ++b)
-      if (b < a) sT[(16 * a + rr) * kLdA + 16 * b + cc] = xv[b];
+      for (int i = 0; i < 16; ++i) {
+        const float d0 = D0[i], d1 = D0[kLdA + i];
+        const float2 t = *reinterpret_cast<const float2*>(Xc + i * kLdA);
+        acc[0] = fmaf(d0, t.x, acc[0]);
+        acc[1] = fmaf(d0, t.y, acc[1]);
+        acc[2] = fmaf(d1, t.x, acc[2]);
+        acc[3] = fmaf(d1, t.y, acc[3]);
+      }
+    }
+    __syncthreads();
+    if (active) {
+      *reinterpret_cast<float2*>(Xab) = make_float2(-acc[0], -acc[1]);
+      *reinterpret_cast<float2*>(Xab + kLdA) = make_float2(-acc[2], -acc[3]);
+    }
     __syncthreads();
   }
 }
 
-// Store 8 consecutive tokens (t0..t0+7) of channel c as tf32 into a K-major
-// [128 channels][64 tokens] tile (the transposed layout of key-side factors).
-__device__ __forceinline__ void st_tf32_col8(unsigned char* tile, int c, int t0, const float (&v)[8]) {
-  uint4 u0, u1;
-  u0.x = f32_to_tf32_rn(v[0]); u0.y = f32_to_tf32_rn(v[1]);
-  u0.z = f32_to_tf32_rn(v[2]); u0.w = f32_to_tf32_rn(v[3]);
-  u1.x = f32_to_tf32_rn(v[4]); u1.y = f32_to_tf32_rn(v[5]);
-  u1.z = f32_to_tf32_rn(v[6]); u1.w = f32_to_tf32_rn(v[7]);
-  *reinterpret_cast<uint4*>(tile + sw128_offset(D, c, 4 * t0)) = u0;
-  *reinterpret_cast<uint4*>(tile + sw128_offset(D, c, 4 * t0 + 16)) = u1;
-}
+// Per-thread values of one chunk kept between steps: this thread's tokens
+// 4w .. 4w+3 (w = warp) and channels 4l .. 4l+3 (l = lane).
+struct ChunkRegs {
+  float e[4][4];    // e^{g - G} (G = the strip's anchor)
+  uint2 kraw[4];    // k (4 bf16)
+  uint2 qraw[4];    // q (4 bf16)
+  float eG[4];      // e^{G}
+  float eglG[4];    // e^{g_last - G}
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -247,11 +250,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   float* sBeta = reinterpret_cast<float*>(sm + kBeta);
   unsigned char* R = sm + kR;
   unsigned char* KG = sm + kKG;
-  float* sAkk = reinterpret_cast<float*>(R + 49152);
-  float* sTp = reinterpret_cast<float*>(R + 49152 + kScr);
+  unsigned char* KP = sm + kKP;
+  float* sAkk = reinterpret_cast<float*>(R + kRAkk);
 
   const int64_t n_chunks = (sg.t1 - sg.t0 + C - 1) / C;
   const uint32_t qkl_bytes = kOut ? 65536u : 49152u;
+  const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, column quarter
+  const int r0 = 4 * warp;                      // this thread's tokens r0 .. r0+3
+  const int strip = warp >> 3;                  // their 32-token strip
 
   if (tid == 0) {
     mbar_init(bar_qkl, 1);
@@ -287,15 +293,29 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     tma_load_3d(sm + kRawV, &maps.v, 0, h, t, bar_v);
     tma_load_3d(sm + kRawV + 8192, &maps.v, 64, h, t, bar_v);
   };
+  auto flag_timeout = [&]() {
+    atomicOr(a.err, kDevErrTimeout);
+    *s_abort = 1;
+  };
+  uint32_t mma_par = 0;
+  auto wait_mma = [&]() {
+    if (!mbar_wait(bar_mma, mma_par)) flag_timeout();
+    mma_par ^= 1u;
+    tc_fence_after();
+  };
+  auto chunk_valid = [&](int64_t m) -> int {
+    const int64_t rem = sg.t1 - (sg.t0 + m * C);
+    return rem < C ? static_cast<int>(rem) : C;
+  };
+
   if (tid == 0 && n_chunks > 0) {
     issue_qkl(sg.t0);
     if (has_v) issue_v(sg.t0);
   }
-  float beta_next = 0.f;
-  if (tid < C && sg.t0 + tid < sg.t1) beta_next = a.beta[(sg.t0 + tid) * H + h];
+  float beta_reg = 0.f;  // beta of the next chunk to be scanned (threads < 64)
+  if (tid < C && sg.t0 + tid < sg.t1) beta_reg = a.beta[(sg.t0 + tid) * H + h];
 
   // ---- initial state, transposed into TMEM: S^T[j][c] = S_init[c][j]
-  const int quad = warp & 3, half = warp >> 2;
   {
     const int j = 32 * quad + lane;
     const float* src = nullptr;
@@ -306,71 +326,60 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         src = a.entry_state + (static_cast<int64_t>(seg_id) * H + h) * D * D;
     }
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 16) {
+    for (int cc = 0; cc < 32; cc += 16) {
       uint32_t r[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
-        const int c = 64 * half + cc + x;
+        const int c = 32 * part + cc + x;
         float v = 0.f;
         if (ident) v = (c == j) ? 1.f : 0.f;
         else if (src) v = src[c * D + j];
         r[x] = __float_as_uint(v);
       }
-      tmem_st16(tmem_addr(tmem, 32 * quad, kColS + 64 * half + cc), r);
+      tmem_st16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), r);
     }
     tmem_wait_st();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
-  uint32_t mma_par = 0;
-  // bounded wait on the MMA barrier by every thread; false = give up
-  auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait(bar_mma, mma_par);
-    mma_par ^= 1u;
-    if (!ok) { atomicOr(a.err, kDevErrTimeout); *s_abort = 1; }
-    tc_fence_after();
-    return ok;
-  };
-
-  const int r0 = 8 * warp;      // this thread's tokens r0 .. r0+7 (phases 1, 5, 7)
-  const int strip = warp >> 2;  // their 32-token strip
-  for (int64_t ci = 0; ci < n_chunks; ++ci) {
-    const int64_t c0 = sg.t0 + ci * C;
-    const int valid = (sg.t1 - c0) < C ? static_cast<int>(sg.t1 - c0) : C;
-
-    // ================= phase 1: decay scan and operand build
-    {
-      const bool ok = mbar_wait(bar_qkl, static_cast<uint32_t>(ci & 1));
-      if (!ok) { atomicOr(a.err, kDevErrTimeout); *s_abort = 1; }
-    }
-    float e[8][4];   // e^{g - G_strip}, kept for phases 5 and 7
-    uint2 kraw[8], qraw[8];
+  ChunkRegs cr;
+  // Decay scan and operand build of chunk m: raw q, k, log_alpha (TMA) ->
+  // registers -> strip operands and k e^g (transposed) in SMEM.  Ends with the
+  // operands visible to the tensor core.  Also prefetches beta of chunk m+1
+  // and starts the TMA of chunk m+1's raw q, k, log_alpha.
+  auto scan_and_build = [&](int64_t m) {
+    const int valid = chunk_valid(m);
+    if (!mbar_wait(bar_qkl, static_cast<uint32_t>(m & 1))) flag_timeout();
+    float g[4][4];
     {
       float run[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int r = r0 + i;
-        const float4 l4 = ld_f32x4(sm + kRawL, r, lane);
         const bool ok = r < valid;
+        const float4 l4 =
+            *reinterpret_cast<const float4*>(sm + kRawL + sw128_offset(C, r, 16 * lane));
         run[0] += ok ? clamp_log_alpha(l4.x) : 0.f;
         run[1] += ok ? clamp_log_alpha(l4.y) : 0.f;
         run[2] += ok ? clamp_log_alpha(l4.z) : 0.f;
         run[3] += ok ? clamp_log_alpha(l4.w) : 0.f;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) e[i][x] = run[x];  // local prefix for now
-        kraw[i] = ok ? ld_bf16x4(sm + kRawK, r, lane) : make_uint2(0u, 0u);
-        qraw[i] = (kOut && ok) ? ld_bf16x4(sm + kRawQ, r, lane) : make_uint2(0u, 0u);
+        for (int x = 0; x < 4; ++x) g[i][x] = run[x];
+        cr.kraw[i] = ok ? *reinterpret_cast<const uint2*>(sm + kRawK + sw128_offset(C, r, 8 * lane))
+                        : make_uint2(0u, 0u);
+        cr.qraw[i] = (kOut && ok)
+                         ? *reinterpret_cast<const uint2*>(sm + kRawQ + sw128_offset(C, r, 8 * lane))
+                         : make_uint2(0u, 0u);
       }
       *reinterpret_cast<float4*>(sTot + warp * 128 + 4 * lane) =
           make_float4(run[0], run[1], run[2], run[3]);
     }
-    if (tid < C) sBeta[tid] = beta_next;
+    if (tid < C) sBeta[tid] = beta_reg;
     __syncthreads();
-    if (*s_abort) break;
-    // raw q, k, log_alpha are in registers now: stream in the next chunk's
-    if (tid == 0 && ci + 1 < n_chunks) issue_qkl(c0 + C);
+    if (tid == 0 && m + 1 < n_chunks) issue_qkl(sg.t0 + (m + 1) * C);
+    if (tid < C) {
+      const int64_t t = sg.t0 + (m + 1) * C + tid;
+      beta_reg = t < sg.t1 ? a.beta[t * H + h] : 0.f;
+    }
     {
       float off[4] = {0.f, 0.f, 0.f, 0.f};
       for (int w = 0; w < warp; ++w) {
@@ -378,78 +387,100 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         off[0] += t4.x; off[1] += t4.y; off[2] += t4.z; off[3] += t4.w;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) e[i][x] += off[x];  // now g
-      // anchors: token 15 (warp 1), token 47 (warp 5), last token 63 (warp 7)
-      float* dst = warp == 1 ? sG0 : warp == 5 ? sG1 : warp == 7 ? sGl : nullptr;
+        for (int x = 0; x < 4; ++x) g[i][x] += off[x];
+      // anchors: token 15 (warp 3), token 47 (warp 11), last token 63 (warp 15)
+      float* dst = warp == 3 ? sG0 : warp == 11 ? sG1 : warp == 15 ? sGl : nullptr;
       if (dst)
-        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(e[7][0], e[7][1], e[7][2], e[7][3]);
-      if (warp == 7)
+        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(g[3][0], g[3][1], g[3][2], g[3][3]);
+      if (warp == 15)
         *reinterpret_cast<float4*>(sEGl + 4 * lane) =
-            make_float4(__expf(e[7][0]), __expf(e[7][1]), __expf(e[7][2]), __expf(e[7][3]));
+            make_float4(__expf(g[3][0]), __expf(g[3][1]), __expf(g[3][2]), __expf(g[3][3]));
     }
     __syncthreads();
-    float eG[4], eglG[4], e10[4];  // e^{G}, e^{g_last - G}, e^{G1 - G0} (own channels)
+    float e10[4];
     {
       const float4 g0 = *reinterpret_cast<const float4*>(sG0 + 4 * lane);
       const float4 g1 = *reinterpret_cast<const float4*>(sG1 + 4 * lane);
       const float4 gl = *reinterpret_cast<const float4*>(sGl + 4 * lane);
-      const float G[4] = {strip ? g1.x : g0.x, strip ? g1.y : g0.y, strip ? g1.z : g0.z,
-                          strip ? g1.w : g0.w};
+      const float G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
       const float GL[4] = {gl.x, gl.y, gl.z, gl.w};
-      const float D10[4] = {g1.x - g0.x, g1.y - g0.y, g1.z - g0.z, g1.w - g0.w};
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        eG[x] = __expf(G[x]);
-        eglG[x] = __expf(GL[x] - G[x]);
-        e10[x] = __expf(D10[x]);
+        const float G = strip ? G1[x] : G0[x];
+        cr.eG[x] = __expf(G);
+        cr.eglG[x] = __expf(GL[x] - G);
+        e10[x] = __expf(G1[x] - G0[x]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) e[i][x] = __expf(e[i][x] - G[x]);  // within [e^-80, e^80]
+        for (int i = 0; i < 4; ++i) cr.e[i][x] = __expf(g[i][x] - G);  // in [e^-80, e^80]
       }
     }
-    {
-      unsigned char* Aop = R;           // bf16 [128 rows][128]: strip s -> rows 64s + (q | k) * 32 + rr
-      unsigned char* Bop = R + 32768;   // bf16 [96 rows][128]: keys of strip 0 | keys of strip 1
-      float kgT[4][8];                  // k e^g for the transposed store
+    unsigned char* Aop = R;           // bf16 [128][128]: strip s -> rows 64 s + (q: 0 | k: 32) + rr
+    unsigned char* Bop = R + 32768;   // bf16 [96][128]: keys 0..31 (strip-0 anchor) | keys 0..63
+    float kgT[4][4];                  // [channel x][token i] of k e^g
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = r0 + i, rr = r & 31;
-        float kf[4], qf[4], qt[4], kt[4], kh[4];
-        unpack4(kraw[i], kf);
-        unpack4(qraw[i], qf);
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + i, rr = r & 31;
+      float kf[4], qf[4], qt[4], kt[4], kh[4];
+      unpack4(cr.kraw[i], kf);
+      unpack4(cr.qraw[i], qf);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float inv = __frcp_rn(e[i][x]);
-          qt[x] = qf[x] * e[i][x];
-          kt[x] = kf[x] * e[i][x];
-          kh[x] = kf[x] * inv;
-          kgT[x][i] = kt[x] * eG[x];
-        }
-        if (kOut) st_bf16x4(Aop, 128, 64 * strip + rr, lane, qt);
-        st_bf16x4(Aop, 128, 64 * strip + 32 + rr, lane, kt);
-        if (strip == 0) {
-          st_bf16x4(Bop, 96, r, lane, kh);
-          float kh1[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) kh1[x] = kh[x] * e10[x];
-          st_bf16x4(Bop, 96, 32 + r, lane, kh1);
-        } else {
-          st_bf16x4(Bop, 96, 32 + r, lane, kh);
-        }
+      for (int x = 0; x < 4; ++x) {
+        const float inv = rcp_approx(cr.e[i][x]);
+        qt[x] = qf[x] * cr.e[i][x];
+        kt[x] = kf[x] * cr.e[i][x];
+        kh[x] = kf[x] * inv;
+        kgT[x][i] = kt[x] * cr.eG[x];
       }
+      *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + rr, 8 * lane)) = pack4_bf16(qt);
+      *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + 32 + rr, 8 * lane)) =
+          pack4_bf16(kt);
+      if (strip == 0) {
+        float kh1[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) st_tf32_col8(KG, 4 * lane + x, r0, kgT[x]);
-      if (!kOut) {  // summary units have no queries: keep the strip rows finite
-        const float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) st_bf16x4(Aop, 128, 64 * strip + ((r0 + i) & 31), lane, z);
+        for (int x = 0; x < 4; ++x) kh1[x] = kh[x] * e10[x];
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, r, 8 * lane)) = pack4_bf16(kh);
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh1);
+      } else {
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh);
       }
     }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      *reinterpret_cast<uint4*>(KG + sw128_offset(D, 4 * lane + x, 4 * r0)) = pack4_tf32(kgT[x]);
     fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
+  };
 
-    // ================= phase 2: strip products (bf16) -> TMEM
+  // O^T of chunk m (TMEM) -> out, bf16.  Lanes = value channels, columns =
+  // tokens; neighbouring lanes swap one value so each store writes a bf16 pair.
+  auto write_out = [&](int64_t m) {
+    const int valid = chunk_valid(m);
+    const int64_t c0 = sg.t0 + m * C;
+    const int j = 32 * quad + lane;
+    uint32_t ov[16];
+    tmem_ld16(tmem_addr(tmem, 32 * quad, kColO + 16 * part), ov);
+    tmem_wait_ld();
+    const bool odd = lane & 1;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      const float v0 = __uint_as_float(ov[2 * y]), v1 = __uint_as_float(ov[2 * y + 1]);
+      const float send = odd ? v0 : v1;
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      const int t = 16 * part + 2 * y + (odd ? 1 : 0);
+      const float lo = odd ? recv : v0, hi = odd ? v1 : recv;
+      if (t < valid)
+        *reinterpret_cast<uint32_t*>(a.out + ((c0 + t) * H + h) * D + (j & ~1)) = pack_bf16x2(lo, hi);
+    }
+  };
+
+  if (n_chunks > 0) scan_and_build(0);
+  for (int64_t n = 0; n < n_chunks; ++n) {
+    if (*s_abort) break;
+
+    // ---- A: strip products (bf16) -> TMEM  ||  out of chunk n-1
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
@@ -462,97 +493,90 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       }
       mma_commit(bar_mma);
     }
-    __syncwarp();
+    if (kOut && n > 0) write_out(n - 1);
     wait_mma();
     __syncthreads();
     if (*s_abort) break;
 
-    // ================= phase 3: strip read-out, UT transform
-    for (int i = tid; i < C * static_cast<int>(kLdA); i += kThreads) sTp[i] = 0.f;
-    if (warp < 4) {
-      // row L = 32 warp + lane of the strip product: strip s = warp / 2,
-      // warp even = query rows (A_qk), odd = key rows (A_kk); token r.
-      const int s = warp >> 1, is_k = warp & 1;
-      const int r = 32 * s + lane;
-      uint32_t v[64];
-#pragma unroll
-      for (int i = 32; i < 64; ++i) v[i] = 0u;
-      const uint32_t col0 = kColA + (s ? 32u : 0u);
-      const uint32_t ta = tmem_addr(tmem, 32 * warp, col0);
-      tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-      tmem_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-      if (s) {
-        tmem_ld16(ta + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-        tmem_ld16(ta + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
-      }
-      tmem_wait_ld();
-      const int nkeys = s ? 64 : 32;
-      if (!is_k) {
-        if (kOut) {  // A_qk row r, tf32, K-major [r][i], zero above the diagonal
-#pragma unroll
-          for (int l4 = 0; l4 < 16; ++l4) {
-            float f[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const int i = 4 * l4 + x;
-              f[x] = (i <= r && i < nkeys) ? __uint_as_float(v[i]) : 0.f;
-            }
-            st_tf32x4(R, C, r, l4, f);
-          }
-        }
-      } else {
-        const float b = sBeta[r];
-        float* row = sAkk + r * kLdA;
-#pragma unroll
-        for (int l4 = 0; l4 < 16; ++l4) {
-          float f[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int i = 4 * l4 + x;
-            f[x] = (i < r && i < nkeys) ? b * __uint_as_float(v[i]) : 0.f;
-          }
-          *reinterpret_cast<float4*>(row + 4 * l4) = make_float4(f[0], f[1], f[2], f[3]);
-        }
-      }
-    }
-    __syncthreads();
-    unit_lower_inverse(sAkk, sTp, tid);
+    // ---- B: strip read-out, UT transform, T to SMEM
     {
-      // T = T' Diag(beta): row r = tid / 4, columns 16 (tid % 4) .. +16
-      const int r = tid >> 2, i0 = 16 * (tid & 3);
-      unsigned char* Tt = R + 16384;    // tf32 [64][64]
-      unsigned char* Th = R + 32768;    // bf16 [64][64] high part
-      unsigned char* Tl = R + 40960;    // bf16 low part
+      // row L = 32 quad + lane of the strip products: strip s = quad / 2,
+      // query rows (A_qk) for even quad, key rows (A_kk) for odd; token r.
+      const int s = quad >> 1, is_k = quad & 1;
+      const int r = 32 * s + lane;
+      const int nk = s ? 16 : 8;  // keys handled by this warp: [i0, i0 + nk)
+      const int i0 = part * nk;
+      uint32_t v[16];
+      const uint32_t ta = tmem_addr(tmem, 32 * quad, kColA + (s ? 32u : 0u) + i0);
+      if (s) tmem_ld16(ta, v); else tmem_ld8(ta, v);
+      tmem_wait_ld();
+      const float b = sBeta[r];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float f[4], hi[4], lo[4];
+      for (int g4 = 0; g4 < 4; ++g4) {
+        if (g4 * 4 >= nk) break;
+        float f[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
-          const int i = i0 + 4 * q4 + x;
-          f[x] = sTp[r * kLdA + i] * sBeta[i];
-          hi[x] = __bfloat162float(__float2bfloat16_rn(f[x]));
-          lo[x] = f[x] - hi[x];
+          const int i = i0 + 4 * g4 + x;
+          const float val = __uint_as_float(v[4 * g4 + x]);
+          f[x] = is_k ? ((i < r) ? b * val : 0.f) : ((i <= r) ? val : 0.f);
         }
-        const int l4 = (i0 >> 2) + q4;
-        st_tf32x4(Tt, C, r, l4, f);
-        st_bf16x4(Th, C, r, l4, hi);
-        st_bf16x4(Tl, C, r, l4, lo);
+        const int i = i0 + 4 * g4;
+        if (is_k)
+          *reinterpret_cast<float4*>(sAkk + r * kLdA + i) = make_float4(f[0], f[1], f[2], f[3]);
+        else if (kOut)
+          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) = pack4_tf32(f);
+      }
+      if (s == 0) {  // strip-0 rows have no keys >= 32
+        const int iz = 32 + 8 * part;
+        if (is_k) {
+          *reinterpret_cast<float4*>(sAkk + r * kLdA + iz) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(sAkk + r * kLdA + iz + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (kOut) {
+          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz)) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz + 16)) = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
+    __syncthreads();
+    unit_lower_inverse_inplace(sAkk, tid);
+    {
+      // T = T' Diag(beta): row r = tid / 8, columns 8 (tid % 8) .. +8
+      const int r = tid >> 3, q8 = tid & 7;
+      const float4 t0 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8);
+      const float4 t1 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8 + 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * q8);
+      const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * q8 + 4);
+      const float f[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                          t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
+      float hi[8], lo[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        hi[x] = __bfloat162float(__float2bfloat16_rn(f[x]));
+        lo[x] = f[x] - hi[x];
+      }
+      const float f0[4] = {f[0], f[1], f[2], f[3]}, f1[4] = {f[4], f[5], f[6], f[7]};
+      *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8)) = pack4_tf32(f0);
+      *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8 + 16)) = pack4_tf32(f1);
+      *reinterpret_cast<uint4*>(R + kRTh + sw128_offset(C, r, 16 * q8)) =
+          make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                     pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
+      *reinterpret_cast<uint4*>(R + kRTl + sw128_offset(C, r, 16 * q8)) =
+          make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                     pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+    }
     fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
 
-    // ================= phase 4: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)
+    // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
     if (tid == 0) {
       bool ok = true;
-      if (has_v) {
-        ok = mbar_wait(bar_v, static_cast<uint32_t>(ci & 1));
-        if (!ok) { atomicOr(a.err, kDevErrTimeout); *s_abort = 1; }
-      }
+      if (has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
       tc_fence_after();
       if (ok) {
         const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
-        const uint32_t kg = smem_u32(KG), tt = smem_u32(R + 16384);
+        const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
 #pragma unroll
         for (int j = 0; j < C / 8; ++j) {
           const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
@@ -562,52 +586,56 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         if (has_v) {
           const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
           const uint32_t vv = smem_u32(sm + kRawV);
-          const uint32_t th = smem_u32(R + 32768), tl = smem_u32(R + 40960);
+          const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
 #pragma unroll
-          for (int j = 0; j < C / 16; ++j) {
-            const uint64_t ad = smem_desc_sw128(vv + j * 2048, 64 * 128, 1024);
-            mma_f16_ss(tmem + kColU, ad, smem_desc_sw128(th + j * 32, 16, 1024), idu, j > 0);
-          }
+          for (int j = 0; j < C / 16; ++j)
+            mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
+                       smem_desc_sw128(th + j * 32, 16, 1024), idu, j > 0);
 #pragma unroll
-          for (int j = 0; j < C / 16; ++j) {
-            const uint64_t ad = smem_desc_sw128(vv + j * 2048, 64 * 128, 1024);
-            mma_f16_ss(tmem + kColU, ad, smem_desc_sw128(tl + j * 32, 16, 1024), idu, 1);
-          }
+          for (int j = 0; j < C / 16; ++j)
+            mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
+                       smem_desc_sw128(tl + j * 32, 16, 1024), idu, 1);
         }
       }
       mma_commit(bar_mma);
     }
-    __syncwarp();
+    {
+      // K' = k e^{g_last - g} = k e^{G - g} e^{g_last - G}, transposed [c][t]
+      float kp[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float kf[4];
+        unpack4(cr.kraw[i], kf);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) kp[x][i] = kf[x] * rcp_approx(cr.e[i][x]) * cr.eglG[x];
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+        *reinterpret_cast<uint4*>(KP + sw128_offset(D, 4 * lane + x, 4 * r0)) = pack4_tf32(kp[x]);
+    }
     wait_mma();
     __syncthreads();
     if (*s_abort) break;
-    if (tid == 0 && has_v && ci + 1 < n_chunks) issue_v(c0 + C);
+    if (tid == 0 && has_v && n + 1 < n_chunks) issue_v(sg.t0 + (n + 1) * C);
 
-    // ================= phase 5: -W (from W^T in TMEM) and q e^g to SMEM
+    // ---- D: -W (from W^T in TMEM, lane = key channel) and q e^g to SMEM
     {
-      // W^T: lane = key channel c, column = token; this warp: tokens 32 half .. +32
       const int c = 32 * quad + lane;
+      uint32_t w[16];
+      tmem_ld16(tmem_addr(tmem, 32 * quad, kColW + 16 * part), w);
+      tmem_wait_ld();
 #pragma unroll
-      for (int t16 = 0; t16 < 32; t16 += 16) {
-        uint32_t w[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quad, kColW + 32 * half + t16), w);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int r = 32 * half + t16 + x;
-          *reinterpret_cast<uint32_t*>(KG + sw128_offset(C, r, 4 * c)) =
-              f32_to_tf32_rn(-__uint_as_float(w[x]));
-        }
-      }
+      for (int x = 0; x < 16; ++x)
+        *reinterpret_cast<uint32_t*>(KG + sw128_offset(C, 16 * part + x, 4 * c)) =
+            f32_to_tf32_rn(-__uint_as_float(w[x]));
       if (kOut) {
-        unsigned char* QG = R + 16384;  // tf32 [64 tokens][128]
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
           float qf[4], f[4];
-          unpack4(qraw[i], qf);
+          unpack4(cr.qraw[i], qf);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) f[x] = qf[x] * e[i][x] * eG[x];
-          st_tf32x4(QG, C, r0 + i, lane, f);
+          for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * cr.eG[x];
+          *reinterpret_cast<uint4*>(R + kRQ + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
         }
       }
     }
@@ -615,11 +643,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     tc_fence_before();
     __syncthreads();
 
-    // ================= phase 6: U^T -= S^T W^T ; O^T = S^T (q e^g)^T   (A = S^T in TMEM)
+    // ---- E: U^T -= S^T W^T ; O^T = S^T (q e^g)^T   (A = S^T in TMEM)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-      const uint32_t wm = smem_u32(KG), qg = smem_u32(R + 16384);
+      const uint32_t wm = smem_u32(KG), qg = smem_u32(R + kRQ);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j) {
         const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
@@ -634,57 +662,41 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       }
       mma_commit(bar_mma);
     }
-    __syncwarp();
     wait_mma();
     __syncthreads();
     if (*s_abort) break;
 
-    // ================= phase 7: decay S^T columns, round U^T, K' to SMEM
+    // ---- F: decay the columns of S^T by e^{g_last}; round U^T to tf32
     {
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
-        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColS + 64 * half + cc);
+      for (int cc = 0; cc < 32; cc += 16) {
+        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc);
         uint32_t sv[16];
         tmem_ld16(ta, sv);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 16; ++x)
-          sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[64 * half + cc + x]);
+          sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[32 * part + cc + x]);
         tmem_st16(ta, sv);
       }
+      const uint32_t tu = tmem_addr(tmem, 32 * quad, kColU + 16 * part);
+      uint32_t uv[16];
+      tmem_ld16(tu, uv);
+      tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < 32; cc += 16) {
-        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColU + 32 * half + cc);
-        uint32_t uv[16];
-        tmem_ld16(ta, uv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
-        tmem_st16(ta, uv);
-      }
+      for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
+      tmem_st16(tu, uv);
       tmem_wait_st();
-      // K' = k e^{g_last - g} = k (e^{G - g}) e^{g_last - G}, transposed [c][t]
-      float kp[4][8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float kf[4];
-        unpack4(kraw[i], kf);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) kp[x][i] = kf[x] * __frcp_rn(e[i][x]) * eglG[x];
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x) st_tf32_col8(KG, 4 * lane + x, r0, kp[x]);
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ================= phase 8: O^T += U^T A_qk^T ; S^T += U^T K'   (A = U^T in TMEM)
+    // ---- G: O^T += U^T A_qk^T ; S^T += U^T K'  (A = U^T)  ||  chunk n+1 operands
     if (tid == 0) {
       tc_fence_after();
       if (kOut) {
         const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-        const uint32_t aq = smem_u32(R);
+        const uint32_t aq = smem_u32(R + kRAqk);
 #pragma unroll
         for (int j = 0; j < C / 8; ++j) {
           const uint64_t bd = smem_desc_sw128(aq + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
@@ -692,7 +704,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         }
       }
       const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-      const uint32_t kp = smem_u32(KG);
+      const uint32_t kp = smem_u32(KP);
 #pragma unroll
       for (int j = 0; j < C / 8; ++j) {
         const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
@@ -700,38 +712,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       }
       mma_commit(bar_mma);
     }
-    if (tid < C) beta_next = (c0 + C + tid < sg.t1) ? a.beta[(c0 + C + tid) * H + h] : 0.f;
-    __syncwarp();
+    if (n + 1 < n_chunks) scan_and_build(n + 1);
     wait_mma();
-    __syncthreads();
-    if (*s_abort) break;
-
-    // ================= phase 9: O^T -> out (bf16)
-    if (kOut) {
-      uint16_t* so = reinterpret_cast<uint16_t*>(R + 16384);  // [64 tokens][128] plain rows
-      const int j = 32 * quad + lane;
-#pragma unroll
-      for (int t16 = 0; t16 < 32; t16 += 16) {
-        uint32_t ov[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quad, kColO + 32 * half + t16), ov);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          so[(32 * half + t16 + x) * D + j] = f32_to_bf16(__uint_as_float(ov[x]));
-      }
-      __syncthreads();
-      const int r = tid >> 2, qtr = tid & 3;  // row, 64-byte quarter
-      if (r < valid) {
-        const uint4* srcv = reinterpret_cast<const uint4*>(so + r * D + 32 * qtr);
-        uint4* dstv = reinterpret_cast<uint4*>(a.out + ((c0 + r) * H + h) * D + 32 * qtr);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) dstv[x] = srcv[x];
-      }
-    }
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
   }
+
+  if (kOut && n_chunks > 0 && !*s_abort) write_out(n_chunks - 1);
 
   // ---- the segment's final state (S^T in TMEM) to global memory
   if (!*s_abort) {
@@ -746,12 +733,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     if (dst) {
       const int j = 32 * quad + lane;
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
+      for (int cc = 0; cc < 32; cc += 16) {
         uint32_t sv[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 64 * half + cc), sv);
+        tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dst[(64 * half + cc + x) * ld + j] = __uint_as_float(sv[x]);
+        for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
       }
     }
   }
@@ -801,9 +788,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 
 template <int MODE>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
-  if (a.T <= 0 || a.T > 0x7fffffffLL) {
-    if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;
-  }
+  if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
   memset(&maps, 0, sizeof maps);
   if (a.T > 0) {
