@@ -39,9 +39,9 @@
 //   B  strip read-out, UT transform (in place), T to SMEM
 //   C  W^T, U~^T MMAs (n)                || K' (n) to SMEM
 //   D  -W and q e^g to SMEM
-//   E  U^T -= S^T W^T ; O^T = S^T (q e^g)^T
+//   E  U^T -= S^T W^T ; O^T = S^T (q e^g)^T || decay scan of chunk n+1
 //   F  decay the columns of S^T, round U^T to tf32 (in TMEM)
-//   G  O^T += U^T A_qk^T ; S^T += U^T K' || decay scan + operands of chunk n+1
+//   G  O^T += U^T A_qk^T ; S^T += U^T K' || operands of chunk n+1 to SMEM
 // Raw q, k, log_alpha stream in by TMA one chunk ahead; v after step C.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -60,8 +60,9 @@ using namespace sm100;
 
 constexpr int D = 128;          // dk = dv
 constexpr int C = kChunk;       // 64
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWorkers = 512;                 // 16 worker warps
+constexpr int kWarps = kWorkers / 32;
+constexpr int kThreads = kWorkers + 32;       // + 1 control warp (MMA issue)
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map (fp32 columns; 128 lanes)
@@ -91,13 +92,15 @@ constexpr uint32_t kMisc = kKP + 32768;
 // f32 warp totals [16][128] of the decay scan: live only in the first half of
 // the operand build, inside the (then unused) strip-B operand area of R
 constexpr uint32_t kTot = kR + 40960;
-constexpr uint32_t kG0 = kMisc;
+constexpr uint32_t kG0 = kMisc;              // anchors g_15, g_47, g_63 [128] each
 constexpr uint32_t kG1 = kG0 + 512;
 constexpr uint32_t kGl = kG1 + 512;
-constexpr uint32_t kEGl = kGl + 512;
-constexpr uint32_t kBeta = kEGl + 512;
-constexpr uint32_t kBars = kBeta + 256;       // 3 mbarriers, TMEM slot, abort flag
-constexpr uint32_t kSmemBytes = kBars + 64 + 1024;  // + alignment slack
+constexpr uint32_t kEGl = kGl + 512;          // e^{g_last} [2][128], by chunk parity
+constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e^{G0}, e^{G1},
+                                              // e^{g_last - G0}, e^{g_last - G1}, e^{G1 - G0}
+constexpr uint32_t kBeta = kPC + 5 * 512;
+constexpr uint32_t kBars = kBeta + 256;       // 10 mbarriers, TMEM slot, abort flag
+constexpr uint32_t kSmemBytes = kBars + 128 + 1024;  // + alignment slack
 static_assert(kRAkk + C * kLdA * 4 <= kRAqk, "A_kk scratch overlaps A_qk");
 static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -113,6 +116,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
+
+// Barrier among the 16 worker warps only (the control warp never joins it).
+__device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
   f[0] = __uint_as_float(u.x << 16);
@@ -130,15 +136,17 @@ __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
 
 // In place: sA holds a strictly lower-triangular 64 x 64 matrix A (f32, row
 // stride kLdA, zero on and above the diagonal); on return it holds
-// T' = (I + A)^{-1} (unit lower-triangular).  The four 16 x 16 diagonal
-// blocks are inverted by column-oriented forward substitution in registers
-// (one thread per column), then block rows are completed in order:
-// T'_ab = -T'_aa sum_{b <= c < a} A_ac T'_cb, with 2 x 2 register tiles.
-__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, int tid) {
-  float x[16];
+// T' = (I + A)^{-1} (unit lower-triangular).  By doubling:
+//   1. the four 16 x 16 diagonal blocks, by column-oriented forward
+//      substitution in registers (one thread per column);
+//   2. 16 -> 32: T'_{b+1,b} = -T'_{b+1,b+1} A_{b+1,b} T'_{bb} for b = 0, 2;
+//   3. 32 -> 64: T'_(10) = -T'_(11) A_(10) T'_(00) on 32 x 32 halves.
+// Xs is 4 KiB of scratch for the intermediate products.  5 barriers.
+__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __restrict__ Xs, int tid) {
   if (tid < 64) {
     const int b = tid >> 4, j = tid & 15;
     const float* Ab = sA + (16 * b) * kLdA + 16 * b;
+    float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
@@ -147,64 +155,56 @@ __device__ void unit_lower_inverse_inplace(float* __restrict__ sA, int tid) {
 #pragma unroll
       for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * kLdA + i], xi, x[r]);
     }
-  }
-  __syncthreads();
-  if (tid < 64) {
-    const int b = tid >> 4, j = tid & 15;
+    __syncwarp();  // every lane of this warp has read its block of A
     float* Tb = sA + (16 * b) * kLdA + 16 * b;
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tb[r * kLdA + j] = x[r];
   }
-  __syncthreads();
-  const int blk = tid >> 6, loc = tid & 63;
-  const int rr = 2 * (loc >> 3), cc = 2 * (loc & 7);
-  for (int a = 1; a < 4; ++a) {
-    const bool active = blk < a;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
-      const int b = blk;
-      for (int c = b; c < a; ++c) {
-        const float* A0 = sA + (16 * a + rr) * kLdA + 16 * c;
-        const float* Tc = sA + (16 * c) * kLdA + 16 * b + cc;
+  worker_sync();
+  {
+    // 16 -> 32: thread = (half h, row r, column c) of a 16 x 16 block
+    const int h = tid >> 8, r = (tid >> 4) & 15, c = tid & 15;
+    const int a = 2 * h + 1, b = 2 * h;
+    const float* Arow = sA + (16 * a + r) * kLdA + 16 * b;
+    const float* Dcol = sA + (16 * b) * kLdA + 16 * b + c;
+    float x = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a0 = A0[i], a1 = A0[kLdA + i];
-          const float2 t = *reinterpret_cast<const float2*>(Tc + i * kLdA);
-          acc[0] = fmaf(a0, t.x, acc[0]);
-          acc[1] = fmaf(a0, t.y, acc[1]);
-          acc[2] = fmaf(a1, t.x, acc[2]);
-          acc[3] = fmaf(a1, t.y, acc[3]);
-        }
-      }
-    }
-    __syncthreads();
-    float* Xab = sA + (16 * a + rr) * kLdA + 16 * blk + cc;
-    if (active) {
-      *reinterpret_cast<float2*>(Xab) = make_float2(acc[0], acc[1]);
-      *reinterpret_cast<float2*>(Xab + kLdA) = make_float2(acc[2], acc[3]);
-    }
-    __syncthreads();
-    if (active) {
-      const float* D0 = sA + (16 * a + rr) * kLdA + 16 * a;
-      const float* Xc = sA + (16 * a) * kLdA + 16 * blk + cc;
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    for (int i = 0; i < 16; ++i) x = fmaf(Arow[i], Dcol[i * kLdA], x);  // A_ab D_b
+    Xs[h * 256 + r * 16 + c] = x;
+    worker_sync();
+    const float* Drow = sA + (16 * a + r) * kLdA + 16 * a;
+    float y = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float d0 = D0[i], d1 = D0[kLdA + i];
-        const float2 t = *reinterpret_cast<const float2*>(Xc + i * kLdA);
-        acc[0] = fmaf(d0, t.x, acc[0]);
-        acc[1] = fmaf(d0, t.y, acc[1]);
-        acc[2] = fmaf(d1, t.x, acc[2]);
-        acc[3] = fmaf(d1, t.y, acc[3]);
-      }
-    }
-    __syncthreads();
-    if (active) {
-      *reinterpret_cast<float2*>(Xab) = make_float2(-acc[0], -acc[1]);
-      *reinterpret_cast<float2*>(Xab + kLdA) = make_float2(-acc[2], -acc[3]);
-    }
-    __syncthreads();
+    for (int i = 0; i < 16; ++i) y = fmaf(Drow[i], Xs[h * 256 + i * 16 + c], y);  // D_a X
+    sA[(16 * a + r) * kLdA + 16 * b + c] = -y;
   }
+  worker_sync();
+  {
+    // 32 -> 64: thread = (rows 2 q, 2 q + 1; column c) of a 32 x 32 block
+    const int q = tid >> 5, c = tid & 31;
+    const float* A0 = sA + (32 + 2 * q) * kLdA;  // rows of A_(10), columns 0..31
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const float t = sA[i * kLdA + c];  // T'_(00)
+      x0 = fmaf(A0[i], t, x0);
+      x1 = fmaf(A0[kLdA + i], t, x1);
+    }
+    Xs[(2 * q) * 32 + c] = x0;
+    Xs[(2 * q + 1) * 32 + c] = x1;
+    worker_sync();
+    const float* T0 = sA + (32 + 2 * q) * kLdA + 32;  // rows of T'_(11)
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const float xv = Xs[i * 32 + c];
+      y0 = fmaf(T0[i], xv, y0);
+      y1 = fmaf(T0[kLdA + i], xv, y1);
+    }
+    sA[(32 + 2 * q) * kLdA + c] = -y0;
+    sA[(33 + 2 * q) * kLdA + c] = -y1;
+  }
+  worker_sync();
 }
 
 // Per-thread values of one chunk kept between steps: this thread's tokens
@@ -213,9 +213,24 @@ struct ChunkRegs {
   float e[4][4];    // e^{g - G} (G = the strip's anchor)
   uint2 kraw[4];    // k (4 bf16)
   uint2 qraw[4];    // q (4 bf16)
-  float eG[4];      // e^{G}
-  float eglG[4];    // e^{g_last - G}
 };
+
+// Stores 4 channel vectors (channels 4 lane + x, x = 0..3; 4 tokens each) of a
+// transposed [128 channel][64 token] tf32 tile.  The order of x is rotated by
+// lane so the 8 rows written by each quarter-warp differ in (row mod 8), i.e.
+// land in different 16-byte swizzle slots: no bank conflicts.
+__device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, int t0,
+                                               const uint4 (&v)[4]) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int x = (s + (lane >> 1)) & 3;
+    uint4 u = v[0];
+    if (x == 1) u = v[1];
+    if (x == 2) u = v[2];
+    if (x == 3) u = v[3];
+    *reinterpret_cast<uint4*>(tile + sw128_offset(D, 4 * lane + x, 4 * t0)) = u;
+  }
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -237,11 +252,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   constexpr bool kOut = MODE == kModeReplay;
   const int H = a.H;
 
-  uint64_t* bar_qkl = reinterpret_cast<uint64_t*>(sm + kBars);
-  uint64_t* bar_v = bar_qkl + 1;
-  uint64_t* bar_mma = bar_qkl + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_qkl + 3);
-  int* s_abort = reinterpret_cast<int*>(tslot + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  uint64_t* bar_qkl = bars + 0;    // raw q, k, log_alpha of a chunk landed (TMA)
+  uint64_t* bar_v = bars + 1;      // raw v landed (TMA)
+  uint64_t* bar_done = bars + 2;   // [4] MMA group committed: 0 strip, 1 WY, 2 S-read, 3 state
+  uint64_t* bar_ready = bars + 6;  // [4] operands of that group ready (one arrive per worker warp)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   float* sTot = reinterpret_cast<float*>(sm + kTot);
   float* sG0 = reinterpret_cast<float*>(sm + kG0);
   float* sG1 = reinterpret_cast<float*>(sm + kG1);
@@ -262,11 +279,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   if (tid == 0) {
     mbar_init(bar_qkl, 1);
     mbar_init(bar_v, 1);
-    mbar_init(bar_mma, 1);
+    for (int g = 0; g < 4; ++g) {
+      mbar_init(bar_done + g, 1);
+      mbar_init(bar_ready + g, kWarps);
+    }
     *s_abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0) {
+  if (warp == kWarps) {  // the control warp owns the TMEM allocation
     tmem_alloc(tslot, kTmemCols);
     tmem_relinquish();
   }
@@ -297,11 +317,16 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     atomicOr(a.err, kDevErrTimeout);
     *s_abort = 1;
   };
-  uint32_t mma_par = 0;
-  auto wait_mma = [&]() {
-    if (!mbar_wait(bar_mma, mma_par)) flag_timeout();
-    mma_par ^= 1u;
+  // worker side: wait for MMA group g of chunk n; signal that group g's operands are ready
+  auto wait_done = [&](int g, int64_t n) {
+    if (!mbar_wait(bar_done + g, static_cast<uint32_t>(n & 1))) flag_timeout();
     tc_fence_after();
+  };
+  auto signal_ready = [&](int g) {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_ready + g);
   };
   auto chunk_valid = [&](int64_t m) -> int {
     const int64_t rem = sg.t1 - (sg.t0 + m * C);
@@ -315,8 +340,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   float beta_reg = 0.f;  // beta of the next chunk to be scanned (threads < 64)
   if (tid < C && sg.t0 + tid < sg.t1) beta_reg = a.beta[(sg.t0 + tid) * H + h];
 
-  // ---- initial state, transposed into TMEM: S^T[j][c] = S_init[c][j]
-  {
+  // ---- initial state, transposed into TMEM: S^T[j][c] = S_init[c][j] (worker warps)
+  if (warp < kWarps) {
     const int j = 32 * quad + lane;
     const float* src = nullptr;
     if (MODE == kModeReplay) {
@@ -342,11 +367,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   }
 
   ChunkRegs cr;
-  // Decay scan and operand build of chunk m: raw q, k, log_alpha (TMA) ->
-  // registers -> strip operands and k e^g (transposed) in SMEM.  Ends with the
-  // operands visible to the tensor core.  Also prefetches beta of chunk m+1
-  // and starts the TMA of chunk m+1's raw q, k, log_alpha.
-  auto scan_and_build = [&](int64_t m) {
+  float* sPC = reinterpret_cast<float*>(sm + kPC);
+  // Decay scan of chunk m: raw q, k, log_alpha (TMA) -> registers (cr), the
+  // strip anchors, the per-channel factors (sPC, e^{g_last} by parity) and
+  // beta (sBeta).  Touches no operand buffer, so it can run while the tensor
+  // core still reads the previous chunk's operands.  Starts the TMA of chunk
+  // m+1's raw q, k, log_alpha once chunk m's are in registers.
+  auto scan_chunk = [&](int64_t m) {
     const int valid = chunk_valid(m);
     if (!mbar_wait(bar_qkl, static_cast<uint32_t>(m & 1))) flag_timeout();
     float g[4][4];
@@ -374,7 +401,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           make_float4(run[0], run[1], run[2], run[3]);
     }
     if (tid < C) sBeta[tid] = beta_reg;
-    __syncthreads();
+    worker_sync();
     if (tid == 0 && m + 1 < n_chunks) issue_qkl(sg.t0 + (m + 1) * C);
     if (tid < C) {
       const int64_t t = sg.t0 + (m + 1) * C + tid;
@@ -394,30 +421,45 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       float* dst = warp == 3 ? sG0 : warp == 11 ? sG1 : warp == 15 ? sGl : nullptr;
       if (dst)
         *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(g[3][0], g[3][1], g[3][2], g[3][3]);
-      if (warp == 15)
-        *reinterpret_cast<float4*>(sEGl + 4 * lane) =
-            make_float4(__expf(g[3][0]), __expf(g[3][1]), __expf(g[3][2]), __expf(g[3][3]));
     }
-    __syncthreads();
-    float e10[4];
-    {
+    worker_sync();
+    if (warp == 0) {  // per-channel factors, once per chunk
       const float4 g0 = *reinterpret_cast<const float4*>(sG0 + 4 * lane);
       const float4 g1 = *reinterpret_cast<const float4*>(sG1 + 4 * lane);
       const float4 gl = *reinterpret_cast<const float4*>(sGl + 4 * lane);
-      const float G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
-      const float GL[4] = {gl.x, gl.y, gl.z, gl.w};
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float G = strip ? G1[x] : G0[x];
-        cr.eG[x] = __expf(G);
-        cr.eglG[x] = __expf(GL[x] - G);
-        e10[x] = __expf(G1[x] - G0[x]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) cr.e[i][x] = __expf(g[i][x] - G);  // in [e^-80, e^80]
-      }
+      float* egl = sEGl + (m & 1) * 128;
+      *reinterpret_cast<float4*>(egl + 4 * lane) =
+          make_float4(__expf(gl.x), __expf(gl.y), __expf(gl.z), __expf(gl.w));
+      *reinterpret_cast<float4*>(sPC + 0 * 128 + 4 * lane) =
+          make_float4(__expf(g0.x), __expf(g0.y), __expf(g0.z), __expf(g0.w));
+      *reinterpret_cast<float4*>(sPC + 1 * 128 + 4 * lane) =
+          make_float4(__expf(g1.x), __expf(g1.y), __expf(g1.z), __expf(g1.w));
+      *reinterpret_cast<float4*>(sPC + 2 * 128 + 4 * lane) = make_float4(
+          __expf(gl.x - g0.x), __expf(gl.y - g0.y), __expf(gl.z - g0.z), __expf(gl.w - g0.w));
+      *reinterpret_cast<float4*>(sPC + 3 * 128 + 4 * lane) = make_float4(
+          __expf(gl.x - g1.x), __expf(gl.y - g1.y), __expf(gl.z - g1.z), __expf(gl.w - g1.w));
+      *reinterpret_cast<float4*>(sPC + 4 * 128 + 4 * lane) = make_float4(
+          __expf(g1.x - g0.x), __expf(g1.y - g0.y), __expf(g1.z - g0.z), __expf(g1.w - g0.w));
     }
+    {
+      const float4 gA = *reinterpret_cast<const float4*>((strip ? sG1 : sG0) + 4 * lane);
+      const float G[4] = {gA.x, gA.y, gA.z, gA.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) cr.e[i][x] = __expf(g[i][x] - G[x]);  // in [e^-80, e^80]
+    }
+  };
+
+  // Operand build of the scanned chunk: strip operands (bf16) and k e^g
+  // (transposed, tf32) into SMEM, made visible to the tensor core.  Reads cr
+  // and sPC (written by scan_chunk, separated from here by a barrier).
+  auto build_chunk = [&]() {
     unsigned char* Aop = R;           // bf16 [128][128]: strip s -> rows 64 s + (q: 0 | k: 32) + rr
     unsigned char* Bop = R + 32768;   // bf16 [96][128]: keys 0..31 (strip-0 anchor) | keys 0..63
+    const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
+    const float4 e104 = *reinterpret_cast<const float4*>(sPC + 4 * 128 + 4 * lane);
+    const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w}, e10[4] = {e104.x, e104.y, e104.z, e104.w};
     float kgT[4][4];                  // [channel x][token i] of k e^g
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -431,7 +473,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         qt[x] = qf[x] * cr.e[i][x];
         kt[x] = kf[x] * cr.e[i][x];
         kh[x] = kf[x] * inv;
-        kgT[x][i] = kt[x] * cr.eG[x];
+        kgT[x][i] = kt[x] * eG[x];
       }
       *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + rr, 8 * lane)) = pack4_bf16(qt);
       *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + 32 + rr, 8 * lane)) =
@@ -446,12 +488,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh);
       }
     }
+    uint4 kv[4];
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
-      *reinterpret_cast<uint4*>(KG + sw128_offset(D, 4 * lane + x, 4 * r0)) = pack4_tf32(kgT[x]);
+    for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kgT[x]);
+    st_transposed4(KG, lane, r0, kv);
     fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
   };
 
   // O^T of chunk m (TMEM) -> out, bf16.  Lanes = value channels, columns =
@@ -476,276 +517,307 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
   };
 
-  if (n_chunks > 0) scan_and_build(0);
-  for (int64_t n = 0; n < n_chunks; ++n) {
-    if (*s_abort) break;
-
-    // ---- A: strip products (bf16) -> TMEM  ||  out of chunk n-1
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
-      const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        const uint64_t ad = smem_desc_sw128(a0 + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(b0 + (j >> 2) * (96 * 128) + (j & 3) * 32, 16, 1024);
-        mma_f16_ss(tmem + kColA, ad, bd, id, j > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    if (kOut && n > 0) write_out(n - 1);
-    wait_mma();
-    __syncthreads();
-    if (*s_abort) break;
-
-    // ---- B: strip read-out, UT transform, T to SMEM
-    {
-      // row L = 32 quad + lane of the strip products: strip s = quad / 2,
-      // query rows (A_qk) for even quad, key rows (A_kk) for odd; token r.
-      const int s = quad >> 1, is_k = quad & 1;
-      const int r = 32 * s + lane;
-      const int nk = s ? 16 : 8;  // keys handled by this warp: [i0, i0 + nk)
-      const int i0 = part * nk;
-      uint32_t v[16];
-      const uint32_t ta = tmem_addr(tmem, 32 * quad, kColA + (s ? 32u : 0u) + i0);
-      if (s) tmem_ld16(ta, v); else tmem_ld8(ta, v);
-      tmem_wait_ld();
-      const float b = sBeta[r];
-#pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {
-        if (g4 * 4 >= nk) break;
-        float f[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int i = i0 + 4 * g4 + x;
-          const float val = __uint_as_float(v[4 * g4 + x]);
-          f[x] = is_k ? ((i < r) ? b * val : 0.f) : ((i <= r) ? val : 0.f);
+  // ================= control warp: issues every MMA group once its operands are ready
+  auto control = [&]() {
+    for (int64_t n = 0; n < n_chunks; ++n) {
+      for (int g = 0; g < 4; ++g) {
+        if (*s_abort) break;
+        const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
+        if (!ready) flag_timeout();
+        tc_fence_after();
+        if (!ready || *s_abort) {
+          mma_commit(bar_done + g);  // nothing issued: release the waiting workers
+          continue;
         }
-        const int i = i0 + 4 * g4;
-        if (is_k)
-          *reinterpret_cast<float4*>(sAkk + r * kLdA + i) = make_float4(f[0], f[1], f[2], f[3]);
-        else if (kOut)
-          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) = pack4_tf32(f);
-      }
-      if (s == 0) {  // strip-0 rows have no keys >= 32
-        const int iz = 32 + 8 * part;
-        if (is_k) {
-          *reinterpret_cast<float4*>(sAkk + r * kLdA + iz) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(sAkk + r * kLdA + iz + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else if (kOut) {
-          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz)) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz + 16)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-    }
-    __syncthreads();
-    unit_lower_inverse_inplace(sAkk, tid);
-    {
-      // T = T' Diag(beta): row r = tid / 8, columns 8 (tid % 8) .. +8
-      const int r = tid >> 3, q8 = tid & 7;
-      const float4 t0 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8);
-      const float4 t1 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8 + 4);
-      const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * q8);
-      const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * q8 + 4);
-      const float f[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
-                          t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
-      float hi[8], lo[8];
+        if (g == 0) {
+          tc_fence_after();
+          const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
+          const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        hi[x] = __bfloat162float(__float2bfloat16_rn(f[x]));
-        lo[x] = f[x] - hi[x];
-      }
-      const float f0[4] = {f[0], f[1], f[2], f[3]}, f1[4] = {f[4], f[5], f[6], f[7]};
-      *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8)) = pack4_tf32(f0);
-      *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8 + 16)) = pack4_tf32(f1);
-      *reinterpret_cast<uint4*>(R + kRTh + sw128_offset(C, r, 16 * q8)) =
-          make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
-                     pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
-      *reinterpret_cast<uint4*>(R + kRTl + sw128_offset(C, r, 16 * q8)) =
-          make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
-                     pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
+          for (int j = 0; j < D / 16; ++j) {
+            const uint64_t ad = smem_desc_sw128(a0 + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + (j >> 2) * (96 * 128) + (j & 3) * 32, 16, 1024);
+            mma_f16_ss(tmem + kColA, ad, bd, id, j > 0);
+          }
+          mma_commit(bar_done + 0);
 
-    // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
-    if (tid == 0) {
-      bool ok = true;
-      if (has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
-      tc_fence_after();
-      if (ok) {
-        const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
-        const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
+        } else if (g == 1) {
+          bool ok = true;
+          if (has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+          tc_fence_after();
+          if (ok) {
+            const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
+            const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
 #pragma unroll
-        for (int j = 0; j < C / 8; ++j) {
-          const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(tt + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-          mma_tf32_ss(tmem + kColW, ad, bd, idw, j > 0);
-        }
-        if (has_v) {
-          const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
-          const uint32_t vv = smem_u32(sm + kRawV);
-          const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
+            for (int j = 0; j < C / 8; ++j) {
+              const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(tt + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+              mma_tf32_ss(tmem + kColW, ad, bd, idw, j > 0);
+            }
+            if (has_v) {
+              const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
+              const uint32_t vv = smem_u32(sm + kRawV);
+              const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
 #pragma unroll
-          for (int j = 0; j < C / 16; ++j)
-            mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
-                       smem_desc_sw128(th + j * 32, 16, 1024), idu, j > 0);
+              for (int j = 0; j < C / 16; ++j)
+                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
+                           smem_desc_sw128(th + j * 32, 16, 1024), idu, j > 0);
 #pragma unroll
-          for (int j = 0; j < C / 16; ++j)
-            mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
-                       smem_desc_sw128(tl + j * 32, 16, 1024), idu, 1);
+              for (int j = 0; j < C / 16; ++j)
+                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
+                           smem_desc_sw128(tl + j * 32, 16, 1024), idu, 1);
+            }
+          }
+          mma_commit(bar_done + 1);
+
+        } else if (g == 2) {
+          tc_fence_after();
+          const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
+          const uint32_t wm = smem_u32(KG), qg = smem_u32(R + kRQ);
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j) {
+            const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+            mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, bd, id, (has_v || j > 0) ? 1u : 0u);
+          }
+          if (kOut) {
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) {
+              const uint64_t bd = smem_desc_sw128(qg + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+              mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, bd, id, j > 0);
+            }
+          }
+          mma_commit(bar_done + 2);
+
+        } else {
+          tc_fence_after();
+          if (kOut) {
+            const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
+            const uint32_t aq = smem_u32(R + kRAqk);
+#pragma unroll
+            for (int j = 0; j < C / 8; ++j) {
+              const uint64_t bd = smem_desc_sw128(aq + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+              mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, bd, id, 1);
+            }
+          }
+          const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+          const uint32_t kp = smem_u32(KP);
+#pragma unroll
+          for (int j = 0; j < C / 8; ++j) {
+            const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+            mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, bd, ids, 1);
+          }
+          mma_commit(bar_done + 3);
+
         }
       }
-      mma_commit(bar_mma);
+      if (*s_abort) break;
     }
-    {
-      // K' = k e^{g_last - g} = k e^{G - g} e^{g_last - G}, transposed [c][t]
-      float kp[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float kf[4];
-        unpack4(cr.kraw[i], kf);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) kp[x][i] = kf[x] * rcp_approx(cr.e[i][x]) * cr.eglG[x];
-      }
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-        *reinterpret_cast<uint4*>(KP + sw128_offset(D, 4 * lane + x, 4 * r0)) = pack4_tf32(kp[x]);
-    }
-    wait_mma();
-    __syncthreads();
-    if (*s_abort) break;
-    if (tid == 0 && has_v && n + 1 < n_chunks) issue_v(sg.t0 + (n + 1) * C);
+  };
 
-    // ---- D: -W (from W^T in TMEM, lane = key channel) and q e^g to SMEM
-    {
-      const int c = 32 * quad + lane;
-      uint32_t w[16];
-      tmem_ld16(tmem_addr(tmem, 32 * quad, kColW + 16 * part), w);
-      tmem_wait_ld();
+  if (warp == kWarps) {
+    if (lane == 0) control();
+    __syncwarp();
+  } else {
+    if (n_chunks > 0) {
+      scan_chunk(0);
+      worker_sync();
+      build_chunk();
+      signal_ready(0);  // strip operands of chunk 0
+    }
+    for (int64_t n = 0; n < n_chunks; ++n) {
+      if (*s_abort) break;
+
+      // ---- A: strip products (bf16) -> TMEM  ||  out of chunk n-1
+      if (kOut && n > 0) write_out(n - 1);
+      wait_done(0, n);
+      worker_sync();
+      if (*s_abort) break;
+
+      // ---- B: strip read-out, UT transform, T to SMEM
+      {
+        // row L = 32 quad + lane of the strip products: strip s = quad / 2,
+        // query rows (A_qk) for even quad, key rows (A_kk) for odd; token r.
+        const int s = quad >> 1, is_k = quad & 1;
+        const int r = 32 * s + lane;
+        const int nk = s ? 16 : 8;  // keys handled by this warp: [i0, i0 + nk)
+        const int i0 = part * nk;
+        uint32_t v[16];
+        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColA + (s ? 32u : 0u) + i0);
+        if (s) tmem_ld16(ta, v); else tmem_ld8(ta, v);
+        tmem_wait_ld();
+        const float b = sBeta[r];
 #pragma unroll
-      for (int x = 0; x < 16; ++x)
-        *reinterpret_cast<uint32_t*>(KG + sw128_offset(C, 16 * part + x, 4 * c)) =
-            f32_to_tf32_rn(-__uint_as_float(w[x]));
-      if (kOut) {
+        for (int g4 = 0; g4 < 4; ++g4) {
+          if (g4 * 4 >= nk) break;
+          float f[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int i = i0 + 4 * g4 + x;
+            const float val = __uint_as_float(v[4 * g4 + x]);
+            f[x] = is_k ? ((i < r) ? b * val : 0.f) : ((i <= r) ? val : 0.f);
+          }
+          const int i = i0 + 4 * g4;
+          if (is_k)
+            *reinterpret_cast<float4*>(sAkk + r * kLdA + i) = make_float4(f[0], f[1], f[2], f[3]);
+          else if (kOut)
+            *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) = pack4_tf32(f);
+        }
+        if (s == 0) {  // strip-0 rows have no keys >= 32
+          const int iz = 32 + 8 * part;
+          if (is_k) {
+            *reinterpret_cast<float4*>(sAkk + r * kLdA + iz) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(sAkk + r * kLdA + iz + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else if (kOut) {
+            *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * iz + 16)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      worker_sync();
+      unit_lower_inverse_inplace(sAkk, reinterpret_cast<float*>(R + kRT), tid);
+      {
+        // T = T' Diag(beta): row r = tid / 8, columns 8 (tid % 8) .. +8
+        const int r = tid >> 3, q8 = tid & 7;
+        const float4 t0 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8);
+        const float4 t1 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8 + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * q8);
+        const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * q8 + 4);
+        const float f[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                            t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
+        float hi[8], lo[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          hi[x] = __bfloat162float(__float2bfloat16_rn(f[x]));
+          lo[x] = f[x] - hi[x];
+        }
+        const float f0[4] = {f[0], f[1], f[2], f[3]}, f1[4] = {f[4], f[5], f[6], f[7]};
+        *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8)) = pack4_tf32(f0);
+        *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8 + 16)) = pack4_tf32(f1);
+        *reinterpret_cast<uint4*>(R + kRTh + sw128_offset(C, r, 16 * q8)) =
+            make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                       pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
+        *reinterpret_cast<uint4*>(R + kRTl + sw128_offset(C, r, 16 * q8)) =
+            make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                       pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+      }
+      signal_ready(1);  // T, k e^g, V ready for the WY products
+
+      // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
+      {
+        // K' = k e^{g_last - g} = k e^{G - g} e^{g_last - G}, transposed [c][t]
+        const float4 gl4 = *reinterpret_cast<const float4*>(sPC + (strip ? 3 : 2) * 128 + 4 * lane);
+        const float eglG[4] = {gl4.x, gl4.y, gl4.z, gl4.w};
+        float kp[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float qf[4], f[4];
-          unpack4(cr.qraw[i], qf);
+          float kf[4];
+          unpack4(cr.kraw[i], kf);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * cr.eG[x];
-          *reinterpret_cast<uint4*>(R + kRQ + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
+          for (int x = 0; x < 4; ++x) kp[x][i] = kf[x] * rcp_approx(cr.e[i][x]) * eglG[x];
         }
+        uint4 kv[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kp[x]);
+        st_transposed4(KP, lane, r0, kv);
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
+      wait_done(1, n);
+      worker_sync();
+      if (*s_abort) break;
+      if (tid == 0 && has_v && n + 1 < n_chunks) issue_v(sg.t0 + (n + 1) * C);
 
-    // ---- E: U^T -= S^T W^T ; O^T = S^T (q e^g)^T   (A = S^T in TMEM)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-      const uint32_t wm = smem_u32(KG), qg = smem_u32(R + kRQ);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-        mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, bd, id, (has_v || j > 0) ? 1u : 0u);
-      }
-      if (kOut) {
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          const uint64_t bd = smem_desc_sw128(qg + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-          mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, bd, id, j > 0);
-        }
-      }
-      mma_commit(bar_mma);
-    }
-    wait_mma();
-    __syncthreads();
-    if (*s_abort) break;
-
-    // ---- F: decay the columns of S^T by e^{g_last}; round U^T to tf32
-    {
-#pragma unroll
-      for (int cc = 0; cc < 32; cc += 16) {
-        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc);
-        uint32_t sv[16];
-        tmem_ld16(ta, sv);
+      // ---- D: -W (from W^T in TMEM, lane = key channel) and q e^g to SMEM
+      {
+        const int c = 32 * quad + lane;
+        uint32_t w[16];
+        tmem_ld16(tmem_addr(tmem, 32 * quad, kColW + 16 * part), w);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 16; ++x)
-          sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[32 * part + cc + x]);
-        tmem_st16(ta, sv);
-      }
-      const uint32_t tu = tmem_addr(tmem, 32 * quad, kColU + 16 * part);
-      uint32_t uv[16];
-      tmem_ld16(tu, uv);
-      tmem_wait_ld();
+          *reinterpret_cast<uint32_t*>(KG + sw128_offset(C, 16 * part + x, 4 * c)) =
+              f32_to_tf32_rn(-__uint_as_float(w[x]));
+        if (kOut) {
+          const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
+          const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w};
 #pragma unroll
-      for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
-      tmem_st16(tu, uv);
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- G: O^T += U^T A_qk^T ; S^T += U^T K'  (A = U^T)  ||  chunk n+1 operands
-    if (tid == 0) {
-      tc_fence_after();
-      if (kOut) {
-        const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-        const uint32_t aq = smem_u32(R + kRAqk);
+          for (int i = 0; i < 4; ++i) {
+            float qf[4], f[4];
+            unpack4(cr.qraw[i], qf);
 #pragma unroll
-        for (int j = 0; j < C / 8; ++j) {
-          const uint64_t bd = smem_desc_sw128(aq + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-          mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, bd, id, 1);
+            for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * eG[x];
+            *reinterpret_cast<uint4*>(R + kRQ + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
+          }
         }
       }
-      const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-      const uint32_t kp = smem_u32(KP);
-#pragma unroll
-      for (int j = 0; j < C / 8; ++j) {
-        const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-        mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, bd, ids, 1);
-      }
-      mma_commit(bar_mma);
-    }
-    if (n + 1 < n_chunks) scan_and_build(n + 1);
-    wait_mma();
-    tc_fence_before();
-    __syncthreads();
-  }
+      signal_ready(2);  // -W and q e^g ready
 
-  if (kOut && n_chunks > 0 && !*s_abort) write_out(n_chunks - 1);
+      // ---- E: U^T -= S^T W^T ; O^T = S^T (q e^g)^T (A = S^T in TMEM) || scan of chunk n+1
+      if (n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
+      wait_done(2, n);
+      worker_sync();
+      if (*s_abort) break;
 
-  // ---- the segment's final state (S^T in TMEM) to global memory
-  if (!*s_abort) {
-    float* dst = nullptr;
-    int64_t ld = D;  // row stride of the destination (floats)
-    if (MODE == kModeReplay) {
-      if (last && a.S_final) dst = a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * D * D;
-    } else {
-      ld = 2 * D;  // increment | transition record
-      dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D) + (ident ? D : 0);
-    }
-    if (dst) {
-      const int j = 32 * quad + lane;
+      // ---- F: decay the columns of S^T by e^{g_last}; round U^T to tf32
+      {
 #pragma unroll
-      for (int cc = 0; cc < 32; cc += 16) {
-        uint32_t sv[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
+        for (int cc = 0; cc < 32; cc += 16) {
+          const uint32_t ta = tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc);
+          uint32_t sv[16];
+          tmem_ld16(ta, sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[(n & 1) * 128 + 32 * part + cc + x]);
+          tmem_st16(ta, sv);
+        }
+        const uint32_t tu = tmem_addr(tmem, 32 * quad, kColU + 16 * part);
+        uint32_t uv[16];
+        tmem_ld16(tu, uv);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+        for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
+        tmem_st16(tu, uv);
+        tmem_wait_st();
+      }
+      signal_ready(3);  // S^T decayed, U^T rounded, A_qk and K' in SMEM
+
+      // ---- G: O^T += U^T A_qk^T ; S^T += U^T K'  (A = U^T)  ||  chunk n+1 operand build
+      if (n + 1 < n_chunks) {
+        build_chunk();  // chunk n+1 operands into freed buffers
+        signal_ready(0);
+      }
+      wait_done(3, n);
+      worker_sync();
+    }
+
+    if (kOut && n_chunks > 0 && !*s_abort) write_out(n_chunks - 1);
+
+    // ---- the segment's final state (S^T in TMEM) to global memory
+    if (!*s_abort) {
+      float* dst = nullptr;
+      int64_t ld = D;  // row stride of the destination (floats)
+      if (MODE == kModeReplay) {
+        if (last && a.S_final) dst = a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * D * D;
+      } else {
+        ld = 2 * D;  // increment | transition record
+        dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D) + (ident ? D : 0);
+      }
+      if (dst) {
+        const int j = 32 * quad + lane;
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 16) {
+          uint32_t sv[16];
+          tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+        }
       }
     }
-  }
+  }  // worker warps
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarps) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---- host side: TMA descriptors
