@@ -315,14 +315,20 @@ def time_decode(kb, dec, steps_per_run, warmup, runs=3):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def cpu_sample(p, n_seqs):
-    """The first `n_seqs` sequences of a workload (all heads)."""
+def cpu_sample(p, n_seqs, max_tokens=None):
+    """The first `n_seqs` sequences of a workload (all heads); with
+    `max_tokens`, only the first tokens of the first sequence."""
     from gated_delta_rule_48_gb300 import inputs as kin
     t1 = int(p.cu_seqlens[n_seqs])
+    cu = p.cu_seqlens[:n_seqs + 1].copy()
+    if max_tokens is not None:
+        t1 = min(int(p.cu_seqlens[1]), int(max_tokens))
+        cu = np.array([0, t1], dtype=np.int64)
+        n_seqs = 1
     return dict(q=kin.bf16_bits(p.q[:t1]), k=kin.bf16_bits(p.k[:t1]), v=kin.bf16_bits(p.v[:t1]),
                 log_alpha=p.log_alpha[:t1].numpy(), beta=p.beta[:t1].numpy(),
                 S0=None if p.S0 is None else p.S0[:n_seqs].numpy(),
-                cu=p.cu_seqlens[:n_seqs + 1].copy(), tokens=t1)
+                cu=cu, tokens=t1)
 
 
 def time_oracle(sample, threads):
@@ -353,24 +359,36 @@ def workload_config(p, idx):
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores.
+
+    Each of the K timed steps evaluates the oracle on a bounded sample of the
+    workload -- the first L tokens of sequence 0, all heads -- with L chosen
+    from a short calibration so the whole run takes about a minute.  Under
+    torchrun only rank 0 works and prints; the other ranks exit without work.
+    """
     from gated_delta_rule_48_gb300 import inputs as kin
     import oracle
     if rank != 0:
         return
     oracle.build()
     p = kin.workload(args.workload)
-    n = 1
-    sample = cpu_sample(p, n)
     threads = oracle.default_threads()
-    for _ in range(min(args.warmup, 1)):
-        time_oracle(sample, threads)
-    per = [time_oracle(sample, threads) for _ in range(max(1, min(args.steps, 3)))]
+    calib = cpu_sample(p, 1, max_tokens=128)
+    t_cal = max(time_oracle(calib, threads), 1e-3)
+    rate = calib["tokens"] / t_cal                       # tokens per second, all heads
+    budget = 45.0                                        # seconds for the timed steps
+    L = int(max(64, min(int(p.cu_seqlens[1]), rate * budget / max(1, args.steps))))
+    sample = cpu_sample(p, 1, max_tokens=L)
+    warm = cpu_sample(p, 1, max_tokens=64)
+    for _ in range(args.warmup):
+        time_oracle(warm, threads)
+    per = [time_oracle(sample, threads) for _ in range(args.steps)]
     sec = statistics.mean(per)
     value = sample["tokens"] / sec / 1e6
-    desc = f"sequence 0 of the workload ({sample['tokens']} tokens x {p.H} heads), fp64"
+    desc = (f"first {sample['tokens']} tokens of sequence 0 x {p.H} heads per step, fp64 "
+            "token-by-token recurrence")
     line = {"impl": "reference", "metric": "KDA prefill throughput", "value": value,
-            "unit": "Mtok/s", "n_gpus": world, "steps": len(per), "warmup": min(args.warmup, 1),
+            "unit": "Mtok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(p, args.workload),
