@@ -141,8 +141,10 @@ __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
 //      substitution in registers (one thread per column);
 //   2. 16 -> 32: T'_{b+1,b} = -T'_{b+1,b+1} A_{b+1,b} T'_{bb} for b = 0, 2;
 //   3. 32 -> 64: T'_(10) = -T'_(11) A_(10) T'_(00) on 32 x 32 halves.
-// Xs is 4 KiB of scratch for the intermediate products.  5 barriers.
-__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __restrict__ Xs, int tid) {
+// Xs is scratch for the intermediate products (32 x 36 floats); A10T holds
+// the transposed block A_(10) (A10T[i][r] = A[32 + r][i]).  5 barriers.
+__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __restrict__ Xs,
+                                           const float* __restrict__ A10T, int tid) {
   if (tid < 64) {
     const int b = tid >> 4, j = tid & 15;
     const float* Ab = sA + (16 * b) * kLdA + 16 * b;
@@ -180,29 +182,36 @@ __device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __rest
   }
   worker_sync();
   {
-    // 32 -> 64: thread = (rows 2 q, 2 q + 1; column c) of a 32 x 32 block
-    const int q = tid >> 5, c = tid & 31;
-    const float* A0 = sA + (32 + 2 * q) * kLdA;  // rows of A_(10), columns 0..31
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const float t = sA[i * kLdA + c];  // T'_(00)
-      x0 = fmaf(A0[i], t, x0);
-      x1 = fmaf(A0[kLdA + i], t, x1);
+    // 32 -> 64, exploiting the triangular factors (warp-uniform loop bounds):
+    //   X = A_(10) T'_(00):  X[r][c] = sum_{i >= c} A10[r][i] T'00[i][c]
+    //     warps 0..7: 4 columns c = 4w .. 4w+3 each, lane = row r; A10 is read
+    //     through its transposed copy A10T[i][r] (conflict-free rows).
+    if (tid < 256) {
+      const int w = tid >> 5, r = tid & 31;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int i = 4 * w; i < 32; ++i) {
+        const float av = A10T[i * 32 + r];
+        const float4 t = *reinterpret_cast<const float4*>(sA + i * kLdA + 4 * w);
+        x[0] = fmaf(av, t.x, x[0]);
+        x[1] = fmaf(av, t.y, x[1]);
+        x[2] = fmaf(av, t.z, x[2]);
+        x[3] = fmaf(av, t.w, x[3]);
+      }
+      *reinterpret_cast<float4*>(Xs + r * 36 + 4 * w) = make_float4(x[0], x[1], x[2], x[3]);
     }
-    Xs[(2 * q) * 32 + c] = x0;
-    Xs[(2 * q + 1) * 32 + c] = x1;
     worker_sync();
-    const float* T0 = sA + (32 + 2 * q) * kLdA + 32;  // rows of T'_(11)
+    //   T'_(10) = -T'_(11) X:  row r = 2w, 2w+1 (16 warps), lane = column c,
+    //     T'11[r][i] = 0 for i > r, so the loop stops at the warp's last row.
+    const int w = tid >> 5, c = tid & 31;
+    const float* T0 = sA + (32 + 2 * w) * kLdA + 32;
     float y0 = 0.f, y1 = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const float xv = Xs[i * 32 + c];
+    for (int i = 0; i <= 2 * w + 1; ++i) {
+      const float xv = Xs[i * 36 + c];
       y0 = fmaf(T0[i], xv, y0);
       y1 = fmaf(T0[kLdA + i], xv, y1);
     }
-    sA[(32 + 2 * q) * kLdA + c] = -y0;
-    sA[(33 + 2 * q) * kLdA + c] = -y1;
+    sA[(32 + 2 * w) * kLdA + c] = -y0;
+    sA[(33 + 2 * w) * kLdA + c] = -y1;
   }
   worker_sync();
 }
@@ -657,8 +666,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             f[x] = is_k ? ((i < r) ? b * val : 0.f) : ((i <= r) ? val : 0.f);
           }
           const int i = i0 + 4 * g4;
-          if (is_k)
+          if (is_k) {
             *reinterpret_cast<float4*>(sAkk + r * kLdA + i) = make_float4(f[0], f[1], f[2], f[3]);
+            if (s == 1 && i < 32) {  // transposed copy of A_(10) for the inverse
+              float* a10t = reinterpret_cast<float*>(R + kRT + 8192);
+#pragma unroll
+              for (int x = 0; x < 4; ++x) a10t[(i + x) * 32 + lane] = f[x];
+            }
+          }
           else if (kOut)
             *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) = pack4_tf32(f);
         }
@@ -674,7 +689,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         }
       }
       worker_sync();
-      unit_lower_inverse_inplace(sAkk, reinterpret_cast<float*>(R + kRT), tid);
+      unit_lower_inverse_inplace(sAkk, reinterpret_cast<float*>(R + kRT),
+                               reinterpret_cast<const float*>(R + kRT + 8192), tid);
       {
         // T = T' Diag(beta): row r = tid / 8, columns 8 (tid % 8) .. +8
         const int r = tid >> 3, q8 = tid & 7;
