@@ -62,7 +62,7 @@ constexpr int D = 128;          // dk = dv
 constexpr int C = kChunk;       // 64
 constexpr int kWorkers = 512;                 // 16 worker warps
 constexpr int kWarps = kWorkers / 32;
-constexpr int kThreads = kWorkers + 32;       // + 1 control warp (MMA issue)
+constexpr int kThreads = kWorkers + 64;       // + 2 control warps (MMA issue)
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map (fp32 columns; 128 lanes)
@@ -289,7 +289,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     mbar_init(bar_qkl, 1);
     mbar_init(bar_v, 1);
     for (int g = 0; g < 4; ++g) {
-      mbar_init(bar_done + g, 1);
+      mbar_init(bar_done + g, g == 0 ? 1 : 2);  // groups 1-3: one commit per issuer
       mbar_init(bar_ready + g, kWarps);
     }
     *s_abort = 0;
@@ -526,44 +526,50 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
   };
 
-  // ================= control warp: issues every MMA group once its operands are ready
-  auto control = [&]() {
+  // ================= control warps: issue the MMA groups once their operands are ready.
+  // Issuing a tcgen05.mma costs the issuing thread ~100 cycles, far more than
+  // the tensor pipe needs for these shapes, so the two independent MMA chains
+  // of groups 1-3 are issued by two threads in parallel (issuer 0 and 1,
+  // lane 0 of the two control warps).  Each issuer commits its own chain.
+  auto control = [&](int who) {
     for (int64_t n = 0; n < n_chunks; ++n) {
       for (int g = 0; g < 4; ++g) {
         if (*s_abort) break;
         const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
         if (!ready) flag_timeout();
         tc_fence_after();
-        if (!ready || *s_abort) {
-          mma_commit(bar_done + g);  // nothing issued: release the waiting workers
-          continue;
-        }
+        const bool go = ready && !*s_abort;
         if (g == 0) {
-          tc_fence_after();
-          const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
-          const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
+          if (who == 0) {  // strip products (bf16)
+            if (go) {
+              const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
+              const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
 #pragma unroll
-          for (int j = 0; j < D / 16; ++j) {
-            const uint64_t ad = smem_desc_sw128(a0 + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + (j >> 2) * (96 * 128) + (j & 3) * 32, 16, 1024);
-            mma_f16_ss(tmem + kColA, ad, bd, id, j > 0);
-          }
-          mma_commit(bar_done + 0);
-
-        } else if (g == 1) {
-          bool ok = true;
-          if (has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
-          tc_fence_after();
-          if (ok) {
-            const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
-            const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
-#pragma unroll
-            for (int j = 0; j < C / 8; ++j) {
-              const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(tt + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-              mma_tf32_ss(tmem + kColW, ad, bd, idw, j > 0);
+              for (int j = 0; j < D / 16; ++j) {
+                const uint64_t ad = smem_desc_sw128(a0 + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(b0 + (j >> 2) * (96 * 128) + (j & 3) * 32, 16, 1024);
+                mma_f16_ss(tmem + kColA, ad, bd, id, j > 0);
+              }
             }
-            if (has_v) {
+            mma_commit(bar_done + 0);
+          }
+        } else if (g == 1) {
+          if (who == 0) {  // W^T = (k e^g)^T T^T (tf32)
+            if (go) {
+              const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
+              const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
+#pragma unroll
+              for (int j = 0; j < C / 8; ++j) {
+                const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(tt + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+                mma_tf32_ss(tmem + kColW, ad, bd, idw, j > 0);
+              }
+            }
+          } else {  // U~^T = V^T T^T (bf16 hi + lo), once raw v has landed
+            bool ok = go;
+            if (ok && has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+            tc_fence_after();
+            if (ok && has_v) {
               const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
               const uint32_t vv = smem_u32(sm + kRawV);
               const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
@@ -578,17 +584,18 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             }
           }
           mma_commit(bar_done + 1);
-
         } else if (g == 2) {
-          tc_fence_after();
           const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-          const uint32_t wm = smem_u32(KG), qg = smem_u32(R + kRQ);
+          if (go && who == 0) {  // U^T -= S^T W^T
+            const uint32_t wm = smem_u32(KG);
 #pragma unroll
-          for (int j = 0; j < D / 8; ++j) {
-            const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-            mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, bd, id, (has_v || j > 0) ? 1u : 0u);
+            for (int j = 0; j < D / 8; ++j) {
+              const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
+              mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, bd, id, (has_v || j > 0) ? 1u : 0u);
+            }
           }
-          if (kOut) {
+          if (go && who == 1 && kOut) {  // O^T = S^T (q e^g)^T
+            const uint32_t qg = smem_u32(R + kRQ);
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) {
               const uint64_t bd = smem_desc_sw128(qg + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
@@ -596,10 +603,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             }
           }
           mma_commit(bar_done + 2);
-
         } else {
-          tc_fence_after();
-          if (kOut) {
+          if (go && who == 1 && kOut) {  // O^T += U^T A_qk^T
             const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
             const uint32_t aq = smem_u32(R + kRAqk);
 #pragma unroll
@@ -608,23 +613,24 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
               mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, bd, id, 1);
             }
           }
-          const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-          const uint32_t kp = smem_u32(KP);
+          if (go && who == 0) {  // S^T += U^T K'
+            const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+            const uint32_t kp = smem_u32(KP);
 #pragma unroll
-          for (int j = 0; j < C / 8; ++j) {
-            const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-            mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, bd, ids, 1);
+            for (int j = 0; j < C / 8; ++j) {
+              const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
+              mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, bd, ids, 1);
+            }
           }
           mma_commit(bar_done + 3);
-
         }
       }
       if (*s_abort) break;
     }
   };
 
-  if (warp == kWarps) {
-    if (lane == 0) control();
+  if (warp >= kWarps) {
+    if (lane == 0) control(warp - kWarps);
     __syncwarp();
   } else {
     if (n_chunks > 0) {
