@@ -62,8 +62,13 @@ constexpr int D = 128;          // dk = dv
 constexpr int C = kChunk;       // 64
 constexpr int kWorkers = 512;                 // 16 worker warps
 constexpr int kWarps = kWorkers / 32;
-constexpr int kThreads = kWorkers + 64;       // + 2 control warps (MMA issue)
+constexpr int kThreads = kWorkers + 128;      // + 1 control warpgroup (2 MMA issuers)
 constexpr uint32_t kTmemCols = 512;
+// Registers: launched at kLaunchRegs per thread (5 warps share a sub-partition);
+// the control warpgroup then hands part of its share to the workers (setmaxnreg).
+constexpr uint32_t kLaunchRegs = 96, kWorkerRegs = 104, kCtrlRegs = 64;
+static_assert(kWorkers * kWorkerRegs + 128 * kCtrlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 
 // TMEM column map (fp32 columns; 128 lanes)
 constexpr uint32_t kColS = 0;     // S^T            128 columns
@@ -80,12 +85,14 @@ constexpr uint32_t kRawL = kRawV + 16384;     // f32 [64][128] sw128 (4 blocks)
 constexpr uint32_t kR = kRawL + 32768;        // phase-dependent operand region (72 KiB):
 //   operands: strip A bf16 [128][128] at +0, strip B bf16 [96][128] at +32768
 //   UT:       T tf32 [64][64] at +0, T_hi / T_lo bf16 [64][64] at +16384 / +24576,
-//             A_kk -> T' f32 [64][kLdA] at +32768
+//             A_kk -> T' f32 [64][kLdA] at +32768, scratch 32 x 36 f32 after it
+//             (the transposed block A_(10) sits in the then idle K' buffer)
 //   hand-off: q e^g tf32 [64][128] at +0
 //   always:   A_qk tf32 [64][64] at +57344
 constexpr uint32_t kLdA = 68;                 // padded row stride (floats)
 constexpr uint32_t kRT = 0, kRTh = 16384, kRTl = 24576, kRAkk = 32768, kRQ = 0;
 constexpr uint32_t kRAqk = 57344;
+constexpr uint32_t kRXs = kRAkk + C * kLdA * 4;  // UT scratch, 32 x 36 f32
 constexpr uint32_t kKG = kR + 73728;          // k e^g (transposed) -> -W  tf32
 constexpr uint32_t kKP = kKG + 32768;         // K' (transposed)            tf32
 constexpr uint32_t kMisc = kKP + 32768;
@@ -101,7 +108,7 @@ constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e
 constexpr uint32_t kBeta = kPC + 5 * 512;
 constexpr uint32_t kBars = kBeta + 256;       // 10 mbarriers, TMEM slot, abort flag
 constexpr uint32_t kSmemBytes = kBars + 128 + 1024;  // + alignment slack
-static_assert(kRAkk + C * kLdA * 4 <= kRAqk, "A_kk scratch overlaps A_qk");
+static_assert(kRXs + 32 * 36 * 4 <= kRAqk, "UT scratch overlaps A_qk");
 static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -117,7 +124,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
-// Barrier among the 16 worker warps only (the control warp never joins it).
+// Barrier among the 16 worker warps only (the control warps never join it).
 __device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
@@ -134,17 +141,33 @@ __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
                     f32_to_tf32_rn(f[3]));
 }
 
-// In place: sA holds a strictly lower-triangular 64 x 64 matrix A (f32, row
-// stride kLdA, zero on and above the diagonal); on return it holds
-// T' = (I + A)^{-1} (unit lower-triangular).  By doubling:
+// T[r][c] = T'[r][c] beta_c into the three operand copies of T: tf32 (rounded
+// to nearest) [64][64] and the bf16 pair hi + lo, all 128-byte swizzled.
+__device__ __forceinline__ void put_T(unsigned char* __restrict__ R, const float* __restrict__ sBeta,
+                                      int r, int c, float tprime) {
+  const float f = tprime * sBeta[c];
+  *reinterpret_cast<uint32_t*>(R + kRT + sw128_offset(C, r, 4 * c)) = f32_to_tf32_rn(f);
+  const __nv_bfloat16 hi = __float2bfloat16_rn(f);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(f - __bfloat162float(hi));
+  *reinterpret_cast<__nv_bfloat16*>(R + kRTh + sw128_offset(C, r, 2 * c)) = hi;
+  *reinterpret_cast<__nv_bfloat16*>(R + kRTl + sw128_offset(C, r, 2 * c)) = lo;
+}
+
+// UT transform.  sA holds a strictly lower-triangular 64 x 64 matrix A (f32,
+// row stride kLdA, zero on and above the diagonal).  Computes
+// T' = (I + A)^{-1} (unit lower-triangular) by doubling and writes
+// T = T' Diag(beta) into its operand copies (put_T):
 //   1. the four 16 x 16 diagonal blocks, by column-oriented forward
-//      substitution in registers (one thread per column);
-//   2. 16 -> 32: T'_{b+1,b} = -T'_{b+1,b+1} A_{b+1,b} T'_{bb} for b = 0, 2;
-//   3. 32 -> 64: T'_(10) = -T'_(11) A_(10) T'_(00) on 32 x 32 halves.
+//      substitution in registers (one thread per column), in place;
+//   2. 16 -> 32: T'_{b+1,b} = -T'_{b+1,b+1} A_{b+1,b} T'_{bb} for b = 0, 2, in place;
+//   3. 32 -> 64: T'_(10) = -T'_(11) A_(10) T'_(00) on 32 x 32 halves, straight
+//      to T; the finished halves T'_(00), T'_(11) (and the zero T'_(01)) go to T
+//      meanwhile.
 // Xs is scratch for the intermediate products (32 x 36 floats); A10T holds
-// the transposed block A_(10) (A10T[i][r] = A[32 + r][i]).  5 barriers.
-__device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __restrict__ Xs,
-                                           const float* __restrict__ A10T, int tid) {
+// the transposed block A_(10) (A10T[i][r] = A[32 + r][i]).  4 barriers.
+__device__ void ut_transform(float* __restrict__ sA, float* __restrict__ Xs,
+                             const float* __restrict__ A10T, const float* __restrict__ sBeta,
+                             unsigned char* __restrict__ R, int tid) {
   if (tid < 64) {
     const int b = tid >> 4, j = tid & 15;
     const float* Ab = sA + (16 * b) * kLdA + 16 * b;
@@ -186,6 +209,8 @@ __device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __rest
     //   X = A_(10) T'_(00):  X[r][c] = sum_{i >= c} A10[r][i] T'00[i][c]
     //     warps 0..7: 4 columns c = 4w .. 4w+3 each, lane = row r; A10 is read
     //     through its transposed copy A10T[i][r] (conflict-free rows).
+    //   warps 8..15 meanwhile write T for the finished halves: rows 4w' .. 4w'+3
+    //     (w' = w - 8), lane = column.
     if (tid < 256) {
       const int w = tid >> 5, r = tid & 31;
       float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -198,6 +223,15 @@ __device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __rest
         x[3] = fmaf(av, t.w, x[3]);
       }
       *reinterpret_cast<float4*>(Xs + r * 36 + 4 * w) = make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+      const int w8 = (tid >> 5) - 8, c = tid & 31;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 4 * w8 + i;
+        put_T(R, sBeta, r, c, sA[r * kLdA + c]);                           // T'_(00)
+        put_T(R, sBeta, 32 + r, 32 + c, sA[(32 + r) * kLdA + 32 + c]);     // T'_(11)
+        put_T(R, sBeta, r, 32 + c, 0.f);                                   // T'_(01) = 0
+      }
     }
     worker_sync();
     //   T'_(10) = -T'_(11) X:  row r = 2w, 2w+1 (16 warps), lane = column c,
@@ -210,10 +244,9 @@ __device__ void unit_lower_inverse_inplace(float* __restrict__ sA, float* __rest
       y0 = fmaf(T0[i], xv, y0);
       y1 = fmaf(T0[kLdA + i], xv, y1);
     }
-    sA[(32 + 2 * w) * kLdA + c] = -y0;
-    sA[(33 + 2 * w) * kLdA + c] = -y1;
+    put_T(R, sBeta, 32 + 2 * w, c, -y0);
+    put_T(R, sBeta, 33 + 2 * w, c, -y1);
   }
-  worker_sync();
 }
 
 // Per-thread values of one chunk kept between steps: this thread's tokens
@@ -532,6 +565,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   // of groups 1-3 are issued by two threads in parallel (issuer 0 and 1,
   // lane 0 of the two control warps).  Each issuer commits its own chain.
   auto control = [&](int who) {
+    // K-major SW128 operand: 8-row groups 1024 B apart; K step j of a
+    // [blocks][rows][128 B] tile starts at block j / kPerBlk, byte (j % kPerBlk) * 32.
+    auto kmaj = [](uint32_t base, int j, uint32_t block_bytes) {
+      return smem_desc_sw128(base + (j >> 2) * block_bytes + (j & 3) * 32, 16, 1024);
+    };
     for (int64_t n = 0; n < n_chunks; ++n) {
       for (int g = 0; g < 4; ++g) {
         if (*s_abort) break;
@@ -544,12 +582,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             if (go) {
               const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
               const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
-#pragma unroll
-              for (int j = 0; j < D / 16; ++j) {
-                const uint64_t ad = smem_desc_sw128(a0 + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(b0 + (j >> 2) * (96 * 128) + (j & 3) * 32, 16, 1024);
-                mma_f16_ss(tmem + kColA, ad, bd, id, j > 0);
-              }
+#pragma unroll 1
+              for (int j = 0; j < D / 16; ++j)
+                mma_f16_ss(tmem + kColA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
             }
             mma_commit(bar_done + 0);
           }
@@ -558,12 +593,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             if (go) {
               const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
               const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
-#pragma unroll
-              for (int j = 0; j < C / 8; ++j) {
-                const uint64_t ad = smem_desc_sw128(kg + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(tt + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-                mma_tf32_ss(tmem + kColW, ad, bd, idw, j > 0);
-              }
+#pragma unroll 1
+              for (int j = 0; j < C / 8; ++j)
+                mma_tf32_ss(tmem + kColW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
             }
           } else {  // U~^T = V^T T^T (bf16 hi + lo), once raw v has landed
             bool ok = go;
@@ -573,14 +605,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
               const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
               const uint32_t vv = smem_u32(sm + kRawV);
               const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
-#pragma unroll
-              for (int j = 0; j < C / 16; ++j)
-                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
-                           smem_desc_sw128(th + j * 32, 16, 1024), idu, j > 0);
-#pragma unroll
-              for (int j = 0; j < C / 16; ++j)
-                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + j * 2048, 64 * 128, 1024),
-                           smem_desc_sw128(tl + j * 32, 16, 1024), idu, 1);
+#pragma unroll 1
+              for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
+                const int jj = j & 3;
+                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + jj * 2048, 64 * 128, 1024),
+                           smem_desc_sw128((j < 4 ? th : tl) + jj * 32, 16, 1024), idu, j > 0);
+              }
             }
           }
           mma_commit(bar_done + 1);
@@ -588,39 +618,32 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
           if (go && who == 0) {  // U^T -= S^T W^T
             const uint32_t wm = smem_u32(KG);
-#pragma unroll
-            for (int j = 0; j < D / 8; ++j) {
-              const uint64_t bd = smem_desc_sw128(wm + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-              mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, bd, id, (has_v || j > 0) ? 1u : 0u);
-            }
+#pragma unroll 1
+            for (int j = 0; j < D / 8; ++j)
+              mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id,
+                          (has_v || j > 0) ? 1u : 0u);
           }
           if (go && who == 1 && kOut) {  // O^T = S^T (q e^g)^T
             const uint32_t qg = smem_u32(R + kRQ);
-#pragma unroll
-            for (int j = 0; j < D / 8; ++j) {
-              const uint64_t bd = smem_desc_sw128(qg + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-              mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, bd, id, j > 0);
-            }
+#pragma unroll 1
+            for (int j = 0; j < D / 8; ++j)
+              mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, kmaj(qg, j, 64 * 128), id, j > 0);
           }
           mma_commit(bar_done + 2);
         } else {
           if (go && who == 1 && kOut) {  // O^T += U^T A_qk^T
             const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
             const uint32_t aq = smem_u32(R + kRAqk);
-#pragma unroll
-            for (int j = 0; j < C / 8; ++j) {
-              const uint64_t bd = smem_desc_sw128(aq + (j >> 2) * (64 * 128) + (j & 3) * 32, 16, 1024);
-              mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, bd, id, 1);
-            }
+#pragma unroll 1
+            for (int j = 0; j < C / 8; ++j)
+              mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, kmaj(aq, j, 64 * 128), id, 1);
           }
           if (go && who == 0) {  // S^T += U^T K'
             const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
             const uint32_t kp = smem_u32(KP);
-#pragma unroll
-            for (int j = 0; j < C / 8; ++j) {
-              const uint64_t bd = smem_desc_sw128(kp + (j >> 2) * (128 * 128) + (j & 3) * 32, 16, 1024);
-              mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, bd, ids, 1);
-            }
+#pragma unroll 1
+            for (int j = 0; j < C / 8; ++j)
+              mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
           }
           mma_commit(bar_done + 3);
         }
@@ -630,9 +653,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
 
   if (warp >= kWarps) {
-    if (lane == 0) control(warp - kWarps);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    if (warp < kWarps + 2 && lane == 0) control(warp - kWarps);
     __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kWorkerRegs));
     if (n_chunks > 0) {
       scan_chunk(0);
       worker_sync();
@@ -675,7 +700,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           if (is_k) {
             *reinterpret_cast<float4*>(sAkk + r * kLdA + i) = make_float4(f[0], f[1], f[2], f[3]);
             if (s == 1 && i < 32) {  // transposed copy of A_(10) for the inverse
-              float* a10t = reinterpret_cast<float*>(R + kRT + 8192);
+              float* a10t = reinterpret_cast<float*>(KP);
 #pragma unroll
               for (int x = 0; x < 4; ++x) a10t[(i + x) * 32 + lane] = f[x];
             }
@@ -695,33 +720,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         }
       }
       worker_sync();
-      unit_lower_inverse_inplace(sAkk, reinterpret_cast<float*>(R + kRT),
-                               reinterpret_cast<const float*>(R + kRT + 8192), tid);
-      {
-        // T = T' Diag(beta): row r = tid / 8, columns 8 (tid % 8) .. +8
-        const int r = tid >> 3, q8 = tid & 7;
-        const float4 t0 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8);
-        const float4 t1 = *reinterpret_cast<const float4*>(sAkk + r * kLdA + 8 * q8 + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(sBeta + 8 * q8);
-        const float4 b1 = *reinterpret_cast<const float4*>(sBeta + 8 * q8 + 4);
-        const float f[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
-                            t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
-        float hi[8], lo[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          hi[x] = __bfloat162float(__float2bfloat16_rn(f[x]));
-          lo[x] = f[x] - hi[x];
-        }
-        const float f0[4] = {f[0], f[1], f[2], f[3]}, f1[4] = {f[4], f[5], f[6], f[7]};
-        *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8)) = pack4_tf32(f0);
-        *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 32 * q8 + 16)) = pack4_tf32(f1);
-        *reinterpret_cast<uint4*>(R + kRTh + sw128_offset(C, r, 16 * q8)) =
-            make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
-                       pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
-        *reinterpret_cast<uint4*>(R + kRTl + sw128_offset(C, r, 16 * q8)) =
-            make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
-                       pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
-      }
+      ut_transform(sAkk, reinterpret_cast<float*>(R + kRXs), reinterpret_cast<const float*>(KP),
+                   sBeta, R, tid);
       signal_ready(1);  // T, k e^g, V ready for the WY products
 
       // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
@@ -892,6 +892,17 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
                     make_map(&maps.la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32);
     if (!ok) return cudaErrorInvalidValue;
   }
+  // The register split inside the kernel assumes the launch allocation; a
+  // build that allocates fewer registers per thread is not launched (its
+  // setmaxnreg.inc could never be satisfied).
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes fa;
+    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE>);
+    if (ea != cudaSuccess) return ea;
+    launch_regs = fa.numRegs;
+  }
+  if (static_cast<uint32_t>(launch_regs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
