@@ -565,11 +565,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   // of groups 1-3 are issued by two threads in parallel (issuer 0 and 1,
   // lane 0 of the two control warps).  Each issuer commits its own chain.
   auto control = [&](int who) {
-    // K-major SW128 operand: 8-row groups 1024 B apart; K step j of a
-    // [blocks][rows][128 B] tile starts at block j / kPerBlk, byte (j % kPerBlk) * 32.
-    auto kmaj = [](uint32_t base, int j, uint32_t block_bytes) {
-      return smem_desc_sw128(base + (j >> 2) * block_bytes + (j & 3) * 32, 16, 1024);
+    // K-major SW128 operand, 8-row groups 1024 B apart: K step j of a
+    // [blocks][rows][128 B] tile starts at block j / 4, byte (j % 4) * 32.  The
+    // start address is the descriptor's low field, so a step is an add to the
+    // tile's base descriptor.
+    auto kmaj = [](uint64_t base_desc, int j, uint32_t block_bytes) {
+      return base_desc + (((j >> 2) * block_bytes + (j & 3) * 32) >> 4);
     };
+    auto kdesc = [](const void* p) { return smem_desc_sw128(smem_u32(p), 16, 1024); };
     for (int64_t n = 0; n < n_chunks; ++n) {
       for (int g = 0; g < 4; ++g) {
         if (*s_abort) break;
@@ -581,8 +584,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           if (who == 0) {  // strip products (bf16)
             if (go) {
               const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
-              const uint32_t a0 = smem_u32(R), b0 = smem_u32(R + 32768);
-#pragma unroll 1
+              const uint64_t a0 = kdesc(R), b0 = kdesc(R + 32768);
+#pragma unroll 4
               for (int j = 0; j < D / 16; ++j)
                 mma_f16_ss(tmem + kColA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
             }
@@ -592,8 +595,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           if (who == 0) {  // W^T = (k e^g)^T T^T (tf32)
             if (go) {
               const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
-              const uint32_t kg = smem_u32(KG), tt = smem_u32(R + kRT);
-#pragma unroll 1
+              const uint64_t kg = kdesc(KG), tt = kdesc(R + kRT);
+#pragma unroll 4
               for (int j = 0; j < C / 8; ++j)
                 mma_tf32_ss(tmem + kColW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
             }
@@ -603,13 +606,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             tc_fence_after();
             if (ok && has_v) {
               const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
-              const uint32_t vv = smem_u32(sm + kRawV);
-              const uint32_t th = smem_u32(R + kRTh), tl = smem_u32(R + kRTl);
-#pragma unroll 1
+              const uint64_t vv = smem_desc_sw128(smem_u32(sm + kRawV), 64 * 128, 1024);
+              const uint64_t th = kdesc(R + kRTh), tl = kdesc(R + kRTl);
+#pragma unroll 4
               for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
                 const int jj = j & 3;
-                mma_f16_ss(tmem + kColU, smem_desc_sw128(vv + jj * 2048, 64 * 128, 1024),
-                           smem_desc_sw128((j < 4 ? th : tl) + jj * 32, 16, 1024), idu, j > 0);
+                mma_f16_ss(tmem + kColU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
+                           idu, j > 0);
               }
             }
           }
@@ -617,15 +620,15 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         } else if (g == 2) {
           const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
           if (go && who == 0) {  // U^T -= S^T W^T
-            const uint32_t wm = smem_u32(KG);
-#pragma unroll 1
+            const uint64_t wm = kdesc(KG);
+#pragma unroll 4
             for (int j = 0; j < D / 8; ++j)
               mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id,
                           (has_v || j > 0) ? 1u : 0u);
           }
           if (go && who == 1 && kOut) {  // O^T = S^T (q e^g)^T
-            const uint32_t qg = smem_u32(R + kRQ);
-#pragma unroll 1
+            const uint64_t qg = kdesc(R + kRQ);
+#pragma unroll 4
             for (int j = 0; j < D / 8; ++j)
               mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, kmaj(qg, j, 64 * 128), id, j > 0);
           }
@@ -633,15 +636,15 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         } else {
           if (go && who == 1 && kOut) {  // O^T += U^T A_qk^T
             const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-            const uint32_t aq = smem_u32(R + kRAqk);
-#pragma unroll 1
+            const uint64_t aq = kdesc(R + kRAqk);
+#pragma unroll 4
             for (int j = 0; j < C / 8; ++j)
               mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, kmaj(aq, j, 64 * 128), id, 1);
           }
           if (go && who == 0) {  // S^T += U^T K'
             const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-            const uint32_t kp = smem_u32(KP);
-#pragma unroll 1
+            const uint64_t kp = kdesc(KP);
+#pragma unroll 4
             for (int j = 0; j < C / 8; ++j)
               mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
           }
