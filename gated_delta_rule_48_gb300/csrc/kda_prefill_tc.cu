@@ -34,7 +34,8 @@
 // operands are always laid out K-major: the key-side factors k e^g and K' are
 // written transposed, [key channel][token].
 //
-// Schedule of chunk n (512 threads; thread 0 issues MMAs and TMA copies):
+// Schedule of chunk n (16 worker warps; two issuer threads in a control
+// warpgroup issue the MMAs and the TMA copies):
 //   A  strip MMA (n)                     || read O^T (n-1) out of TMEM -> out
 //   B  strip read-out, UT transform (in place), T to SMEM
 //   C  W^T, U~^T MMAs (n)                || K' (n) to SMEM
@@ -106,7 +107,7 @@ constexpr uint32_t kEGl = kGl + 512;          // e^{g_last} [2][128], by chunk p
 constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e^{G0}, e^{G1},
                                               // e^{g_last - G0}, e^{g_last - G1}, e^{G1 - G0}
 constexpr uint32_t kBeta = kPC + 5 * 512;
-constexpr uint32_t kBars = kBeta + 256;       // 10 mbarriers, TMEM slot, abort flag
+constexpr uint32_t kBars = kBeta + 256;       // 11 mbarriers, TMEM slot, abort flag
 constexpr uint32_t kSmemBytes = kBars + 128 + 1024;  // + alignment slack
 static_assert(kRXs + 32 * 36 * 4 <= kRAqk, "UT scratch overlaps A_qk");
 static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
@@ -299,7 +300,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   uint64_t* bar_v = bars + 1;      // raw v landed (TMA)
   uint64_t* bar_done = bars + 2;   // [4] MMA group committed: 0 strip, 1 WY, 2 S-read, 3 state
   uint64_t* bar_ready = bars + 6;  // [4] operands of that group ready (one arrive per worker warp)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* bar_raw = bars + 10;   // raw q, k, log_alpha of a chunk read (one arrive per worker warp)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   float* sTot = reinterpret_cast<float*>(sm + kTot);
   float* sG0 = reinterpret_cast<float*>(sm + kG0);
@@ -325,6 +327,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       mbar_init(bar_done + g, g == 0 ? 1 : 2);  // groups 1-3: one commit per issuer
       mbar_init(bar_ready + g, kWarps);
     }
+    mbar_init(bar_raw, kWarps);
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -375,10 +378,6 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     return rem < C ? static_cast<int>(rem) : C;
   };
 
-  if (tid == 0 && n_chunks > 0) {
-    issue_qkl(sg.t0);
-    if (has_v) issue_v(sg.t0);
-  }
   float beta_reg = 0.f;  // beta of the next chunk to be scanned (threads < 64)
   if (tid < C && sg.t0 + tid < sg.t1) beta_reg = a.beta[(sg.t0 + tid) * H + h];
 
@@ -439,12 +438,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
                          ? *reinterpret_cast<const uint2*>(sm + kRawQ + sw128_offset(C, r, 8 * lane))
                          : make_uint2(0u, 0u);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_raw);  // this warp is done with the raw tiles
       *reinterpret_cast<float4*>(sTot + warp * 128 + 4 * lane) =
           make_float4(run[0], run[1], run[2], run[3]);
     }
     if (tid < C) sBeta[tid] = beta_reg;
     worker_sync();
-    if (tid == 0 && m + 1 < n_chunks) issue_qkl(sg.t0 + (m + 1) * C);
     if (tid < C) {
       const int64_t t = sg.t0 + (m + 1) * C + tid;
       beta_reg = t < sg.t1 ? a.beta[t * H + h] : 0.f;
@@ -573,7 +573,16 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       return base_desc + (((j >> 2) * block_bytes + (j & 3) * 32) >> 4);
     };
     auto kdesc = [](const void* p) { return smem_desc_sw128(smem_u32(p), 16, 1024); };
+    if (who == 1 && n_chunks > 0) {
+      issue_qkl(sg.t0);
+      if (has_v) issue_v(sg.t0);
+    }
     for (int64_t n = 0; n < n_chunks; ++n) {
+      if (who == 1) {  // raw q, k, log_alpha of chunk n read by every worker: stream in n+1
+        if (*s_abort) break;
+        if (!mbar_wait(bar_raw, static_cast<uint32_t>(n & 1))) { flag_timeout(); break; }
+        if (n + 1 < n_chunks) issue_qkl(sg.t0 + (n + 1) * C);
+      }
       for (int g = 0; g < 4; ++g) {
         if (*s_abort) break;
         const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
@@ -617,6 +626,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             }
           }
           mma_commit(bar_done + 1);
+          // raw v of chunk n consumed once group 1 has completed: stream in n+1
+          if (who == 1 && has_v && n + 1 < n_chunks) {
+            if (mbar_wait(bar_done + 1, static_cast<uint32_t>(n & 1))) issue_v(sg.t0 + (n + 1) * C);
+            else flag_timeout();
+          }
         } else if (g == 2) {
           const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
           if (go && who == 0) {  // U^T -= S^T W^T
@@ -748,7 +762,6 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       wait_done(1, n);
       worker_sync();
       if (*s_abort) break;
-      if (tid == 0 && has_v && n + 1 < n_chunks) issue_v(sg.t0 + (n + 1) * C);
 
       // ---- D: -W (from W^T in TMEM, lane = key channel) and q e^g to SMEM
       {
