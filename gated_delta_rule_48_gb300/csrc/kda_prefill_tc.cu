@@ -142,11 +142,9 @@ __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
                     f32_to_tf32_rn(f[3]));
 }
 
-// T[r][c] = T'[r][c] beta_c into the three operand copies of T: tf32 (rounded
-// to nearest) [64][64] and the bf16 pair hi + lo, all 128-byte swizzled.
-__device__ __forceinline__ void put_T(unsigned char* __restrict__ R, const float* __restrict__ sBeta,
-                                      int r, int c, float tprime) {
-  const float f = tprime * sBeta[c];
+// T[r][c] = f (= T'[r][c] beta_c) into the three operand copies of T: tf32
+// (rounded to nearest) [64][64] and the bf16 pair hi + lo, all 128-byte swizzled.
+__device__ __forceinline__ void put_T(unsigned char* __restrict__ R, int r, int c, float f) {
   *reinterpret_cast<uint32_t*>(R + kRT + sw128_offset(C, r, 4 * c)) = f32_to_tf32_rn(f);
   const __nv_bfloat16 hi = __float2bfloat16_rn(f);
   const __nv_bfloat16 lo = __float2bfloat16_rn(f - __bfloat162float(hi));
@@ -208,45 +206,69 @@ __device__ void ut_transform(float* __restrict__ sA, float* __restrict__ Xs,
   {
     // 32 -> 64, exploiting the triangular factors (warp-uniform loop bounds):
     //   X = A_(10) T'_(00):  X[r][c] = sum_{i >= c} A10[r][i] T'00[i][c]
-    //     warps 0..7: 4 columns c = 4w .. 4w+3 each, lane = row r; A10 is read
-    //     through its transposed copy A10T[i][r] (conflict-free rows).
+    //     warps 0..7: 4 columns c = 4q .. 4q+3 each, lane = row r; A10 is read
+    //     through its transposed copy A10T[i][r] (conflict-free rows).  Column
+    //     group q costs 32 - 4q terms; q = w for w < 4, 11 - w above, so each
+    //     SM sub-partition (warps w and w + 4) gets the same work.
     //   warps 8..15 meanwhile write T for the finished halves: rows 4w' .. 4w'+3
     //     (w' = w - 8), lane = column.
     if (tid < 256) {
       const int w = tid >> 5, r = tid & 31;
+      const int q = w < 4 ? w : 11 - w;
       float x[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i = 4 * w; i < 32; ++i) {
-        const float av = A10T[i * 32 + r];
-        const float4 t = *reinterpret_cast<const float4*>(sA + i * kLdA + 4 * w);
-        x[0] = fmaf(av, t.x, x[0]);
-        x[1] = fmaf(av, t.y, x[1]);
-        x[2] = fmaf(av, t.z, x[2]);
-        x[3] = fmaf(av, t.w, x[3]);
+      for (int i0 = 4 * q; i0 < 32; i0 += 4) {  // 4 steps per pass: the loads issue together
+        float av[4];
+        float4 t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          av[u] = A10T[(i0 + u) * 32 + r];
+          t[u] = *reinterpret_cast<const float4*>(sA + (i0 + u) * kLdA + 4 * q);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          x[0] = fmaf(av[u], t[u].x, x[0]);
+          x[1] = fmaf(av[u], t[u].y, x[1]);
+          x[2] = fmaf(av[u], t[u].z, x[2]);
+          x[3] = fmaf(av[u], t[u].w, x[3]);
+        }
       }
-      *reinterpret_cast<float4*>(Xs + r * 36 + 4 * w) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(Xs + r * 36 + 4 * q) = make_float4(x[0], x[1], x[2], x[3]);
     } else {
       const int w8 = (tid >> 5) - 8, c = tid & 31;
+      const float b0 = sBeta[c], b1 = sBeta[32 + c];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = 4 * w8 + i;
-        put_T(R, sBeta, r, c, sA[r * kLdA + c]);                           // T'_(00)
-        put_T(R, sBeta, 32 + r, 32 + c, sA[(32 + r) * kLdA + 32 + c]);     // T'_(11)
-        put_T(R, sBeta, r, 32 + c, 0.f);                                   // T'_(01) = 0
+        put_T(R, r, c, sA[r * kLdA + c] * b0);                             // T'_(00)
+        put_T(R, 32 + r, 32 + c, sA[(32 + r) * kLdA + 32 + c] * b1);       // T'_(11)
+        // T'_(01) = 0
+        *reinterpret_cast<uint32_t*>(R + kRT + sw128_offset(C, r, 4 * (32 + c))) = 0u;
+        *reinterpret_cast<uint16_t*>(R + kRTh + sw128_offset(C, r, 2 * (32 + c))) = 0u;
+        *reinterpret_cast<uint16_t*>(R + kRTl + sw128_offset(C, r, 2 * (32 + c))) = 0u;
       }
     }
     worker_sync();
-    //   T'_(10) = -T'_(11) X:  row r = 2w, 2w+1 (16 warps), lane = column c,
-    //     T'11[r][i] = 0 for i > r, so the loop stops at the warp's last row.
+    //   T'_(10) = -T'_(11) X:  rows 2p, 2p+1 per warp, lane = column c;
+    //     T'11[r][i] = 0 for i > r, so the loop stops at the warp's last row
+    //     (read 4 entries at a time: the zeros past the diagonal are harmless).
+    //     Row pair p costs 2p + 2 terms; p = k, 7 - k, 8 + k, 15 - k for the
+    //     four warps k, k + 4, k + 8, k + 12 of sub-partition k (equal sums).
     const int w = tid >> 5, c = tid & 31;
-    const float* T0 = sA + (32 + 2 * w) * kLdA + 32;
+    const int k4 = w & 3, j4 = w >> 2;
+    const int p = j4 == 0 ? k4 : j4 == 1 ? 7 - k4 : j4 == 2 ? 8 + k4 : 15 - k4;
+    const float* T0 = sA + (32 + 2 * p) * kLdA + 32;
     float y0 = 0.f, y1 = 0.f;
-    for (int i = 0; i <= 2 * w + 1; ++i) {
-      const float xv = Xs[i * 36 + c];
-      y0 = fmaf(T0[i], xv, y0);
-      y1 = fmaf(T0[kLdA + i], xv, y1);
+    for (int i0 = 0; i0 <= 2 * p + 1; i0 += 4) {
+      const float4 a0 = *reinterpret_cast<const float4*>(T0 + i0);
+      const float4 a1 = *reinterpret_cast<const float4*>(T0 + kLdA + i0);
+      const float xv0 = Xs[i0 * 36 + c], xv1 = Xs[(i0 + 1) * 36 + c];
+      const float xv2 = Xs[(i0 + 2) * 36 + c], xv3 = Xs[(i0 + 3) * 36 + c];
+      y0 = fmaf(a0.x, xv0, y0); y0 = fmaf(a0.y, xv1, y0); y0 = fmaf(a0.z, xv2, y0); y0 = fmaf(a0.w, xv3, y0);
+      y1 = fmaf(a1.x, xv0, y1); y1 = fmaf(a1.y, xv1, y1); y1 = fmaf(a1.z, xv2, y1); y1 = fmaf(a1.w, xv3, y1);
     }
-    put_T(R, sBeta, 32 + 2 * w, c, -y0);
-    put_T(R, sBeta, 33 + 2 * w, c, -y1);
+    const float bc = sBeta[c];
+    put_T(R, 32 + 2 * p, c, -y0 * bc);
+    put_T(R, 33 + 2 * p, c, -y1 * bc);
   }
 }
 
