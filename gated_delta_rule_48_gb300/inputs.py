@@ -218,3 +218,94 @@ def make_decode(N, H, dk, dv=None, steps=64, *, seed=4, s_std=0.02, name="") -> 
 
 def decode_workload(steps=64) -> DecodeInputs:
     return make_decode(256, 32, 128, steps=steps, seed=4, name=WORKLOADS[4])
+
+
+# ---------------------------------------------------------------- raw inputs
+# For the entry points that prepare their inputs on load (kda_chunk_fwd_fused,
+# kda_decode_step_fused): q and k are NOT normalised and the decay arrives as a
+# gate logit.  Draws: q, k, v ~ N(0, 1) and gate ~ N(0, 1) in float32, each
+# rounded to bfloat16 (nearest even); beta = sigmoid(N(0, 1)) float32; S0 as
+# in make_prefill.  The gate's N(0, 1) is the input of the workloads'
+# -5 * sigmoid curve; applying that curve is the layer's job here, not this
+# module's.
+
+@dataclass
+class RawPrefillInputs:
+    q_raw: torch.Tensor      # bf16 [total_T, H, dk], unnormalised
+    k_raw: torch.Tensor      # bf16 [total_T, H, dk], unnormalised
+    v: torch.Tensor          # bf16 [total_T, H, dv]
+    gate: torch.Tensor       # bf16 [total_T, H, dk], logits
+    beta: torch.Tensor       # f32 [total_T, H]
+    S0: torch.Tensor | None  # f32 [N, H, dk, dv]
+    cu_seqlens: np.ndarray   # int64 [N + 1]
+    name: str = ""
+
+    @property
+    def total_T(self) -> int:
+        return int(self.q_raw.shape[0])
+
+    @property
+    def n_seqs(self) -> int:
+        return int(self.cu_seqlens.shape[0] - 1)
+
+    @property
+    def H(self) -> int:
+        return int(self.q_raw.shape[1])
+
+    @property
+    def dk(self) -> int:
+        return int(self.q_raw.shape[2])
+
+    @property
+    def dv(self) -> int:
+        return int(self.v.shape[2])
+
+
+def make_prefill_raw(seq_lens, H, dk, dv=None, *, seed=0, s0_std=0.0, q_scale=1.0,
+                     name="") -> RawPrefillInputs:
+    """Seeded raw prefill inputs (draw order q, k, v, gate, beta, S0).
+
+    ``q_scale`` multiplies the q draw before rounding (the layer's
+    normalisation must make the result independent of it)."""
+    dv = dk if dv is None else dv
+    seq_lens = [int(x) for x in seq_lens]
+    total_T = sum(seq_lens)
+    rng = np.random.default_rng(seed)
+    q = _to_bf16(_normal_blocks(rng, total_T, (H, dk)) * np.float32(q_scale), False)
+    k = _to_bf16(_normal_blocks(rng, total_T, (H, dk)), False)
+    v = _to_bf16(_normal_blocks(rng, total_T, (H, dv)), False)
+    gate = _to_bf16(_normal_blocks(rng, total_T, (H, dk)), False)
+    b = _sigmoid(_normal_blocks(rng, total_T, (H,)))
+    N = len(seq_lens)
+    S0 = None
+    if s0_std:
+        S0 = torch.from_numpy(
+            (rng.standard_normal((N, H, dk, dv), dtype=np.float32) * np.float32(s0_std)))
+    cu = np.zeros(N + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(seq_lens)
+    return RawPrefillInputs(q_raw=q, k_raw=k, v=v, gate=gate,
+                            beta=torch.from_numpy(np.ascontiguousarray(b)), S0=S0,
+                            cu_seqlens=cu, name=name)
+
+
+@dataclass
+class RawDecodeInputs:
+    q_raw: torch.Tensor      # bf16 [steps, N, H, dk]
+    k_raw: torch.Tensor      # bf16 [steps, N, H, dk]
+    v: torch.Tensor          # bf16 [steps, N, H, dv]
+    gate: torch.Tensor       # bf16 [steps, N, H, dk]
+    beta: torch.Tensor       # f32 [steps, N, H]
+    S: torch.Tensor          # f32 [N, H, dk, dv]
+    name: str = ""
+
+
+def make_decode_raw(N, H, dk, dv=None, steps=8, *, seed=5, s_std=0.02, name="") -> RawDecodeInputs:
+    """Raw per-step decode inputs, drawn like a raw prefill of steps * N tokens [steps, N]."""
+    dv = dk if dv is None else dv
+    p = make_prefill_raw([steps * N], H, dk, dv, seed=seed)
+    rng = np.random.default_rng(seed + 1000)
+    S = torch.from_numpy(rng.standard_normal((N, H, dk, dv), dtype=np.float32)
+                         * np.float32(s_std))
+    return RawDecodeInputs(q_raw=p.q_raw.view(steps, N, H, dk), k_raw=p.k_raw.view(steps, N, H, dk),
+                           v=p.v.view(steps, N, H, dv), gate=p.gate.view(steps, N, H, dk),
+                           beta=p.beta.view(steps, N, H), S=S, name=name)
