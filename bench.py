@@ -44,6 +44,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fused", action="store_true")
     return ap.parse_args()
 
 
@@ -53,6 +54,14 @@ def prefill_bytes(n_token_heads, n_seq_heads, d, has_s0):
     """q, k, v (bf16), log_alpha (f32), beta (f32) read, out (bf16) written per
     token-head; S0 read (if given) and S_final written per sequence-head."""
     per_th = 3 * 2 * d + 4 * d + 4 + 2 * d
+    per_sh = 4 * d * d * (2 if has_s0 else 1)
+    return n_token_heads * per_th + n_seq_heads * per_sh
+
+
+def prefill_bytes_fused(n_token_heads, n_seq_heads, d, has_s0):
+    """The fused entry point: raw q, k, v and the gate logits (all bf16), beta
+    (f32) read, out (bf16) written per token-head; the state as above."""
+    per_th = 4 * 2 * d + 4 + 2 * d
     per_sh = 4 * d * d * (2 if has_s0 else 1)
     return n_token_heads * per_th + n_seq_heads * per_sh
 
@@ -243,6 +252,37 @@ def time_prefill(kb, p, steps, warmup, world):
     kernels = kb.profile_read()
     ms = start.elapsed_time(stop) / steps
     return ms, kernels, clocks.summary()
+
+
+def time_prefill_fused(kb, r, steps, warmup):
+    """Device-resident raw inputs; K timed kda_chunk_fwd_fused calls.  Returns
+    (ms per step, per-kernel tracing)."""
+    q, k, v, g = r.q_raw.cuda(), r.k_raw.cuda(), r.v.cuda(), r.gate.cuda()
+    b = r.beta.cuda()
+    S0 = None if r.S0 is None else r.S0.cuda()
+    out = torch.empty((r.total_T, r.H, r.dv), dtype=torch.bfloat16, device="cuda")
+    S = torch.empty((r.n_seqs, r.H, r.dk, r.dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kb.kda_chunk_fwd_fused(q, k, v, g, b, S0, None, out=out, S_final=S, n_seqs=r.n_seqs,
+                               stream=stream)
+
+    for _ in range(warmup):
+        step()
+    if kb.kda_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    kb.profile_read()
+    kb.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    kb.profile_enable(False)
+    return start.elapsed_time(stop) / steps, kb.profile_read()
 
 
 def time_prefill_e2e(kb, p, steps, warmup):
@@ -460,6 +500,28 @@ def main():
         line["e2e"] = {"value": tokens_all / (e2e_ms * 1e-3) / 1e6, "unit": "Mtok/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_ms}
+
+    if not args.no_fused and p.uniform:
+        # the same batch shape through the entry point that prepares its inputs on
+        # load (raw q, k projections, bf16 gate logits)
+        T_b = p.total_T // p.n_seqs
+        r = kin.make_prefill_raw([T_b] * p.n_seqs, p.H, d, seed=100 + args.workload,
+                                 s0_std=0.02 if p.S0 is not None else 0.0)
+        fms, fk = time_prefill_fused(kb, r, max(3, min(args.steps, 50)), args.warmup)
+        fbytes = prefill_bytes_fused(th, sh, d, r.S0 is not None)
+        fn, ft = fk["kda_prefill_replay"]
+        f_gbs = fbytes * (max(3, min(args.steps, 50)) / fn) / (ft / fn * 1e-3) / 1e9
+        line["fused_prep"] = {
+            "workload": workload_config(p, args.workload)["workload"]
+                        + ", raw projections (unnormalised q, k; bf16 gate logits)",
+            "value": p.total_T / (fms * 1e-3) / 1e6, "unit": "Mtok/s", "ms_per_step": fms,
+            "roofline": {"bound": "hbm", "achieved": f_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": f_gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("kda_prefill_replay_fused", "kda_prefill_tc.cu"),
+                         "kernel": "kda_prefill_replay", "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": fbytes}}
+        line["gpu_launches_fused"] = sum(n for n, _ in fk.values())
+        del r
 
     if not args.no_decode:
         dec = kin.decode_workload(steps=args.decode_steps)

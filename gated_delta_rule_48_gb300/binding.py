@@ -102,6 +102,10 @@ def load():
             lib.kda_chunk_fwd_noalloc.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
             lib.kda_decode_step.restype = ctypes.c_int
             lib.kda_decode_step.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
+            lib.kda_chunk_fwd_fused.restype = ctypes.c_int
+            lib.kda_chunk_fwd_fused.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
+            lib.kda_decode_step_fused.restype = ctypes.c_int
+            lib.kda_decode_step_fused.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int
             lib.kda_get_device_error.argtypes = [vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -146,7 +150,7 @@ def _require(t, dtype, name):
 
 def kda_chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, out=None,
                   S_final=None, *, n_seqs=None, segment_tokens=0, want_state=True,
-                  stream=None):
+                  stream=None, _fused=False):
     """Prefill.  Tensors in the packed layout of ``include/kda.h``.
 
     q, k: bf16 [T, H, dk] (or [B, T_b, H, dk], a uniform batch); v bf16;
@@ -166,8 +170,9 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, out=None,
         n_seqs = cu_seqlens.shape[0] - 1
     elif n_seqs is None:
         n_seqs = 1
+    la_dt, la_name = (torch.bfloat16, "gate") if _fused else (torch.float32, "log_alpha")
     for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
-                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (v, torch.bfloat16, "v"), (log_alpha, la_dt, la_name),
                         (beta, torch.float32, "beta"), (S0, torch.float32, "S0"),
                         (cu_seqlens, torch.int32, "cu_seqlens")):
         _require(t, dt, name)
@@ -180,11 +185,24 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, out=None,
     lib = load()
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
             _ptr(cu_seqlens), _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv]
-    if segment_tokens:
+    if _fused:
+        if segment_tokens:
+            raise ValueError("the fused entry point chooses its own segments")
+        _check(lib.kda_chunk_fwd_fused(*args, _stream(stream)))
+    elif segment_tokens:
         _check(lib.kda_chunk_fwd_split(*args, int(segment_tokens), _stream(stream)))
     else:
         _check(lib.kda_chunk_fwd(*args, _stream(stream)))
     return out, S_final
+
+
+def kda_chunk_fwd_fused(q_raw, k_raw, v, gate, beta, S0=None, cu_seqlens=None, out=None,
+                        S_final=None, *, n_seqs=None, want_state=True, stream=None):
+    """Prefill with the input preparation on load: q_raw, k_raw bf16 unnormalised,
+    gate bf16 logits [T, H, dk] in place of log_alpha (log alpha = -5 sigmoid(gate)).
+    Otherwise as :func:`kda_chunk_fwd`."""
+    return kda_chunk_fwd(q_raw, k_raw, v, gate, beta, S0, cu_seqlens, out, S_final,
+                         n_seqs=n_seqs, want_state=want_state, stream=stream, _fused=True)
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S_inout, out=None, *, stream=None):
@@ -204,6 +222,23 @@ def kda_decode_step(q, k, v, log_alpha, beta, S_inout, out=None, *, stream=None)
     _require(out, torch.bfloat16, "out")
     _check(load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                   _ptr(S_inout), _ptr(out), N, H, dk, dv, _stream(stream)))
+    return out
+
+
+def kda_decode_step_fused(q_raw, k_raw, v, gate, beta, S_inout, out=None, *, stream=None):
+    """Decode step with the input preparation on load (see :func:`kda_chunk_fwd_fused`)."""
+    N, H, dk = q_raw.shape
+    dv = v.shape[-1]
+    for t, dt, name in ((q_raw, torch.bfloat16, "q_raw"), (k_raw, torch.bfloat16, "k_raw"),
+                        (v, torch.bfloat16, "v"), (gate, torch.bfloat16, "gate"),
+                        (beta, torch.float32, "beta"), (S_inout, torch.float32, "S_inout")):
+        _require(t, dt, name)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=torch.bfloat16, device=q_raw.device)
+    _require(out, torch.bfloat16, "out")
+    _check(load().kda_decode_step_fused(_ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(gate),
+                                        _ptr(beta), _ptr(S_inout), _ptr(out), N, H, dk, dv,
+                                        _stream(stream)))
     return out
 
 

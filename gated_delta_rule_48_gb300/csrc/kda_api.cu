@@ -163,12 +163,15 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
   return L;
 }
 
+// fused = false: q, k normalised by the caller, log_alpha f32.  fused = true:
+// q, k raw, and `log_alpha` points at the bf16 gate logits instead.
 static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
-                                 const float* log_alpha, const float* beta,
+                                 const void* log_alpha, const float* beta,
                                  const float* S0, const int32_t* cu_seqlens, void* out,
                                  float* S_final, int64_t T, int32_t N, int32_t H,
-                                 int32_t dk, int32_t dv, int64_t segment_tokens,
+                                 int32_t dk, int32_t dv, int64_t segment_tokens, bool fused,
                                  void* stream_v) {
+  const char* la_name = fused ? "gate" : "log_alpha";
   // ---- host-side checks: nothing is launched unless all pass
   if (T < 0 || N < 0 || H <= 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "total_tokens=%lld n_seqs=%d n_heads=%d",
@@ -185,19 +188,19 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                 (long long)segment_tokens, kChunk);
   if (T > 0) {
     const struct { const void* p; const char* n; } req[] = {
-        {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, "log_alpha"}, {beta, "beta"}, {out, "out"}};
+        {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, la_name}, {beta, "beta"}, {out, "out"}};
     for (auto& r : req)
       if (!r.p) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", r.n);
   }
   const void* all[] = {q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final};
-  const char* names[] = {"q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"};
+  const char* names[] = {"q", "k", "v", la_name, "beta", "S0", "cu_seqlens", "out", "S_final"};
   for (int i = 0; i < 9; ++i)
     if (misaligned(all[i])) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", names[i]);
   const int64_t qk_bytes = T * H * dk * 2, v_bytes = T * H * dv * 2;
-  const int64_t la_bytes = T * H * dk * 4, b_bytes = T * H * 4;
+  const int64_t la_bytes = T * H * dk * (fused ? 2 : 4), b_bytes = T * H * 4;
   const int64_t s_bytes = static_cast<int64_t>(N) * H * dk * dv * 4;
   Range in[] = {range_of("q", q, qk_bytes), range_of("k", k, qk_bytes), range_of("v", v, v_bytes),
-                range_of("log_alpha", log_alpha, la_bytes), range_of("beta", beta, b_bytes),
+                range_of(la_name, log_alpha, la_bytes), range_of("beta", beta, b_bytes),
                 range_of("S0", S0, S0 ? s_bytes : 0),
                 range_of("cu_seqlens", cu_seqlens, cu_seqlens ? (N + 1) * 4 : 0)};
   Range r_out = range_of("out", out, T > 0 ? v_bytes : 0);
@@ -244,7 +247,9 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.q = static_cast<const uint16_t*>(q);
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
-  a.log_alpha = log_alpha;
+  a.log_alpha = fused ? nullptr : static_cast<const float*>(log_alpha);
+  a.fused = fused ? 1 : 0;
+  a.gate = fused ? static_cast<const uint16_t*>(log_alpha) : nullptr;
   a.beta = beta;
   a.S0 = S0;
   a.out = static_cast<uint16_t*>(out);
@@ -278,7 +283,16 @@ extern "C" kda_status kda_chunk_fwd(const void* q, const void* k, const void* v,
                                     float* S_final, int64_t total_tokens, int32_t n_seqs,
                                     int32_t n_heads, int32_t dk, int32_t dv, void* stream) {
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
-                        n_seqs, n_heads, dk, dv, 0, stream);
+                        n_seqs, n_heads, dk, dv, 0, false, stream);
+}
+
+extern "C" kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v,
+                                          const void* gate, const float* beta, const float* S0,
+                                          const int32_t* cu_seqlens, void* out, float* S_final,
+                                          int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
+                                          int32_t dk, int32_t dv, void* stream) {
+  return chunk_fwd_impl(q_raw, k_raw, v, gate, beta, S0, cu_seqlens, out, S_final, total_tokens,
+                        n_seqs, n_heads, dk, dv, 0, true, stream);
 }
 
 extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const void* v,
@@ -288,20 +302,21 @@ extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const vo
                                           int32_t n_seqs, int32_t n_heads, int32_t dk,
                                           int32_t dv, int64_t segment_tokens, void* stream) {
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
-                        n_seqs, n_heads, dk, dv, segment_tokens, stream);
+                        n_seqs, n_heads, dk, dv, segment_tokens, false, stream);
 }
 
-extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* v,
-                                      const float* log_alpha, const float* beta,
-                                      float* S_inout, void* out, int32_t N, int32_t H,
-                                      int32_t dk, int32_t dv, void* stream) {
+// fused as in chunk_fwd_impl
+static kda_status decode_impl(const void* q, const void* k, const void* v, const void* log_alpha,
+                              const float* beta, float* S_inout, void* out, int32_t N, int32_t H,
+                              int32_t dk, int32_t dv, bool fused, void* stream) {
+  const char* la_name = fused ? "gate" : "log_alpha";
   if (N < 0 || H <= 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs=%d n_heads=%d", N, H);
   kda_status st = check_head_dims(dk, dv);
   if (st != KDA_OK) return st;
   if (N == 0) return KDA_OK;
   const struct { const void* p; const char* n; } req[] = {
-      {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, "log_alpha"},
+      {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, la_name},
       {beta, "beta"}, {S_inout, "S_inout"}, {out, "out"}};
   for (auto& r : req) {
     if (!r.p) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", r.n);
@@ -310,7 +325,8 @@ extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* 
   const int64_t nh = static_cast<int64_t>(N) * H;
   Range r_out = range_of("out", out, nh * dv * 2);
   Range others[] = {range_of("q", q, nh * dk * 2), range_of("k", k, nh * dk * 2),
-                    range_of("v", v, nh * dv * 2), range_of("log_alpha", log_alpha, nh * dk * 4),
+                    range_of("v", v, nh * dv * 2),
+                    range_of(la_name, log_alpha, nh * dk * (fused ? 2 : 4)),
                     range_of("beta", beta, nh * 4), range_of("S_inout", S_inout, nh * dk * dv * 4)};
   for (auto& r : others)
     if (overlaps(r_out, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps %s", r.name);
@@ -318,11 +334,27 @@ extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* 
     if (overlaps(others[5], others[i]))
       return fail(KDA_ERR_INVALID_ARGUMENT, "S_inout overlaps %s", others[i].name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
-                                static_cast<const uint16_t*>(v), log_alpha, beta, S_inout,
-                                static_cast<uint16_t*>(out), N, H, dk, dv, s);
+  cudaError_t e = launch_decode(
+      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+      static_cast<const uint16_t*>(v), fused ? nullptr : static_cast<const float*>(log_alpha),
+      fused ? static_cast<const uint16_t*>(log_alpha) : nullptr, beta, S_inout,
+      static_cast<uint16_t*>(out), N, H, dk, dv, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KDA_OK;
+}
+
+extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* v,
+                                      const float* log_alpha, const float* beta,
+                                      float* S_inout, void* out, int32_t N, int32_t H,
+                                      int32_t dk, int32_t dv, void* stream) {
+  return decode_impl(q, k, v, log_alpha, beta, S_inout, out, N, H, dk, dv, false, stream);
+}
+
+extern "C" kda_status kda_decode_step_fused(const void* q_raw, const void* k_raw, const void* v,
+                                            const void* gate, const float* beta, float* S_inout,
+                                            void* out, int32_t N, int32_t H, int32_t dk,
+                                            int32_t dv, void* stream) {
+  return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, N, H, dk, dv, true, stream);
 }
 
 extern "C" kda_status kda_get_device_error(void* stream) {

@@ -30,12 +30,14 @@ struct DecodeCfg {
   static constexpr int kRowsPerThread = D / kRowGroups;     // 16 or 8
 };
 
-template <int D>
+// FUSED: q, k arrive raw and are L2-normalised (then rounded to bf16) here,
+// and `gate` (bf16 logits) replaces log_alpha: log alpha = -5 sigmoid(gate).
+template <int D, bool FUSED>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
 decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
               const uint16_t* __restrict__ v, const float* __restrict__ log_alpha,
-              const float* __restrict__ beta, float* __restrict__ S,
-              uint16_t* __restrict__ out) {
+              const uint16_t* __restrict__ gate, const float* __restrict__ beta,
+              float* __restrict__ S, uint16_t* __restrict__ out) {
   using Cfg = DecodeCfg<D>;
   constexpr int CG = Cfg::kColGroups, RG = Cfg::kRowGroups, RPT = Cfg::kRowsPerThread;
   const int64_t unit = blockIdx.x;  // sequence * H + head
@@ -57,9 +59,27 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   for (int c = tid; c < D; c += Cfg::kThreads) {
     s_k[c] = bf16_to_f32(k[vec + c]);
     s_q[c] = bf16_to_f32(q[vec + c]);
-    s_alpha[c] = expf(clamp_log_alpha(log_alpha[vec + c]));
+    s_alpha[c] = expf(FUSED ? gate_log_alpha(bf16_to_f32(gate[vec + c]))
+                            : clamp_log_alpha(log_alpha[vec + c]));
   }
   __syncthreads();
+  if (FUSED) {  // warp 0 normalises k, warp 1 q
+    __shared__ float s_scale[2];
+    if (tid < 64) {
+      const float* x = tid < 32 ? s_k : s_q;
+      float ss = 0.f;
+      for (int c = tid & 31; c < D; c += 32) ss += x[c] * x[c];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if ((tid & 31) == 0) s_scale[tid >> 5] = l2_scale(ss);
+    }
+    __syncthreads();
+    for (int c = tid; c < D; c += Cfg::kThreads) {
+      s_k[c] = bf16_to_f32(f32_to_bf16(s_k[c] * s_scale[0]));
+      s_q[c] = bf16_to_f32(f32_to_bf16(s_q[c] * s_scale[1]));
+    }
+    __syncthreads();
+  }
 
   if (tid < 32) {  // q . k
     float p = 0.f;
@@ -105,19 +125,29 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
 
 }  // namespace
 
+template <int D, bool FUSED>
+void launch_decode_t(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* log_alpha, const uint16_t* gate, const float* beta, float* S,
+                     uint16_t* out, int64_t units, cudaStream_t s) {
+  decode_kernel<D, FUSED><<<static_cast<unsigned>(units), DecodeCfg<D>::kThreads, 0, s>>>(
+      q, k, v, log_alpha, gate, beta, S, out);
+}
+
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                          const float* log_alpha, const float* beta, float* S, uint16_t* out,
-                          int32_t N, int32_t H, int32_t dk, int32_t dv, cudaStream_t s) {
+                          const float* log_alpha, const uint16_t* gate, const float* beta,
+                          float* S, uint16_t* out, int32_t N, int32_t H, int32_t dk, int32_t dv,
+                          cudaStream_t s) {
   (void)dv;  // dk == dv is checked by the caller
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   prof_begin(s, "kda_decode_step");
-  if (dk == 128)
-    decode_kernel<128><<<static_cast<unsigned>(units), DecodeCfg<128>::kThreads, 0, s>>>(
-        q, k, v, log_alpha, beta, S, out);
-  else
-    decode_kernel<64><<<static_cast<unsigned>(units), DecodeCfg<64>::kThreads, 0, s>>>(
-        q, k, v, log_alpha, beta, S, out);
+  if (dk == 128) {
+    if (gate) launch_decode_t<128, true>(q, k, v, log_alpha, gate, beta, S, out, units, s);
+    else launch_decode_t<128, false>(q, k, v, log_alpha, gate, beta, S, out, units, s);
+  } else {
+    if (gate) launch_decode_t<64, true>(q, k, v, log_alpha, gate, beta, S, out, units, s);
+    else launch_decode_t<64, false>(q, k, v, log_alpha, gate, beta, S, out, units, s);
+  }
   prof_end(s, "kda_decode_step");
   return cudaGetLastError();
 }

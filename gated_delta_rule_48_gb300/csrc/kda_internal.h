@@ -54,6 +54,10 @@ struct PrefillArgs {
   float* entry_state;      // [capacity, H, dk, dv]: S_in(j) for j >= 1
   Plan plan;               // segment list in the workspace
   int* err;                // device error word
+  // fused input preparation (kda_chunk_fwd_fused): q, k are raw and are
+  // L2-normalised on load; log alpha comes from the bf16 gate logits
+  int fused = 0;
+  const uint16_t* gate = nullptr;  // bf16 [T, H, dk] when fused
 };
 
 // ---- error reporting shared by the entry points (kda_api.cu)
@@ -79,11 +83,12 @@ cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s);
 
 // ---- decode (kda_decode.cu)
+// gate != null selects the fused input preparation (raw q, k; bf16 gate logits)
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, const float* log_alpha,
-                          const float* beta, float* S, uint16_t* out,
-                          int32_t N, int32_t H, int32_t dk, int32_t dv,
-                          cudaStream_t s);
+                          const uint16_t* gate, const float* beta, float* S,
+                          uint16_t* out, int32_t N, int32_t H, int32_t dk,
+                          int32_t dv, cudaStream_t s);
 
 // bf16 helpers usable from device code without cuda_bf16.h conversions.
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
@@ -99,6 +104,17 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 
 __device__ __forceinline__ float clamp_log_alpha(float la) {
   return fminf(fmaxf(la, kLogAlphaMin), 0.0f);
+}
+
+// ---- fused input preparation (the *_fused entry points)
+// log alpha from a gate logit x: the bounded gate -5 sigmoid(x), then the
+// same clamp as a given log alpha (a no-op for finite x).
+__device__ __forceinline__ float gate_log_alpha(float x) {
+  return clamp_log_alpha(-5.0f * __frcp_rn(1.0f + __expf(-x)));
+}
+// Scale of an L2 normalisation x / max(||x||, 1e-12) from ss = sum of x^2.
+__device__ __forceinline__ float l2_scale(float ss) {
+  return fminf(__frsqrt_rn(ss), 1e12f);
 }
 
 }  // namespace kda

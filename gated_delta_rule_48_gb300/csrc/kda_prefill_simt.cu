@@ -97,7 +97,7 @@ prefill_simt_kernel(PrefillArgs a) {
         const int64_t idx = ((c0 + r) * H + h) * D + c;
         kk = bf16_to_f32(a.k[idx]);
         if (MODE == 1) qq = bf16_to_f32(a.q[idx]);
-        la = clamp_log_alpha(a.log_alpha[idx]);
+        la = a.fused ? gate_log_alpha(bf16_to_f32(a.gate[idx])) : clamp_log_alpha(a.log_alpha[idx]);
       }
       sm.k[r * LD + c] = kk;
       sm.q[r * LD + c] = qq;
@@ -112,6 +112,17 @@ prefill_simt_kernel(PrefillArgs a) {
     for (int r = tid; r < C; r += kThreads)
       sm.beta[r] = r < valid ? a.beta[(c0 + r) * H + h] : 0.f;
     __syncthreads();
+    if (a.fused) {  // raw q, k: L2-normalise each token's row, round to bf16
+      for (int rr = tid; rr < 2 * C; rr += kThreads) {
+        if (rr >= C && MODE != 1) break;
+        float* row = (rr < C ? sm.k : sm.q) + (rr % C) * LD;
+        float ss = 0.f;
+        for (int c = 0; c < D; ++c) ss += row[c] * row[c];
+        const float sc = l2_scale(ss);
+        for (int c = 0; c < D; ++c) row[c] = bf16_to_f32(f32_to_bf16(row[c] * sc));
+      }
+      __syncthreads();
+    }
 
     // ---- cumulative log-decay per channel
     for (int c = tid; c < D; c += kThreads) {

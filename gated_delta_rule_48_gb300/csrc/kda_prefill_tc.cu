@@ -114,7 +114,7 @@ static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan tot
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct TcMaps {
-  CUtensorMap q, k, v, la;
+  CUtensorMap q, k, v, la;  // la: f32 log alpha, or the bf16 gate logits when fused
 };
 
 enum : int { kModeSummary = 0, kModeReplay = 1 };
@@ -137,6 +137,22 @@ __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
 __device__ __forceinline__ uint2 pack4_bf16(const float (&f)[4]) {
   return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
 }
+// Fused input preparation: one token's 128 channels, 4 per lane across the
+// warp, scaled to unit L2 norm (x / max(||x||, 1e-12)) and rounded to bf16.
+// Every lane of the warp must call it.
+__device__ __forceinline__ uint2 l2norm_bf16x4(uint2 raw) {
+  float f[4];
+  f[0] = __uint_as_float(raw.x << 16);
+  f[1] = __uint_as_float(raw.x & 0xffff0000u);
+  f[2] = __uint_as_float(raw.y << 16);
+  f[3] = __uint_as_float(raw.y & 0xffff0000u);
+  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float sc = l2_scale(ss);
+  return make_uint2(pack_bf16x2(f[0] * sc, f[1] * sc), pack_bf16x2(f[2] * sc, f[3] * sc));
+}
+
 __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
   return make_uint4(f32_to_tf32_rn(f[0]), f32_to_tf32_rn(f[1]), f32_to_tf32_rn(f[2]),
                     f32_to_tf32_rn(f[3]));
@@ -297,7 +313,7 @@ __device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, in
   }
 }
 
-template <int MODE>
+template <int MODE, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -337,7 +353,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   float* sAkk = reinterpret_cast<float*>(R + kRAkk);
 
   const int64_t n_chunks = (sg.t1 - sg.t0 + C - 1) / C;
-  const uint32_t qkl_bytes = kOut ? 65536u : 49152u;
+  // raw q (replay only), k, and log alpha (f32) or gate logits (bf16)
+  const uint32_t qkl_bytes = (kOut ? 32768u : 16384u) + (FUSED ? 16384u : 32768u);
   const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, column quarter
   const int r0 = 4 * warp;                      // this thread's tokens r0 .. r0+3
   const int strip = warp >> 3;                  // their 32-token strip
@@ -371,8 +388,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
     tma_load_3d(sm + kRawK, &maps.k, 0, h, t, bar_qkl);
     tma_load_3d(sm + kRawK + 8192, &maps.k, 64, h, t, bar_qkl);
+    if (FUSED) {
+      tma_load_3d(sm + kRawL, &maps.la, 0, h, t, bar_qkl);
+      tma_load_3d(sm + kRawL + 8192, &maps.la, 64, h, t, bar_qkl);
+    } else {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_3d(sm + kRawL + 8192 * b, &maps.la, 32 * b, h, t, bar_qkl);
+      for (int b = 0; b < 4; ++b) tma_load_3d(sm + kRawL + 8192 * b, &maps.la, 32 * b, h, t, bar_qkl);
+    }
   };
   auto issue_v = [&](int64_t c0) {
     mbar_arrive_expect_tx(bar_v, 16384u);
@@ -446,12 +468,22 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       for (int i = 0; i < 4; ++i) {
         const int r = r0 + i;
         const bool ok = r < valid;
-        const float4 l4 =
-            *reinterpret_cast<const float4*>(sm + kRawL + sw128_offset(C, r, 16 * lane));
-        run[0] += ok ? clamp_log_alpha(l4.x) : 0.f;
-        run[1] += ok ? clamp_log_alpha(l4.y) : 0.f;
-        run[2] += ok ? clamp_log_alpha(l4.z) : 0.f;
-        run[3] += ok ? clamp_log_alpha(l4.w) : 0.f;
+        float la[4];
+        if (FUSED) {  // gate logits, bf16
+          float gf[4];
+          unpack4(*reinterpret_cast<const uint2*>(sm + kRawL + sw128_offset(C, r, 8 * lane)), gf);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) la[x] = gate_log_alpha(gf[x]);
+        } else {
+          const float4 l4 =
+              *reinterpret_cast<const float4*>(sm + kRawL + sw128_offset(C, r, 16 * lane));
+          la[0] = clamp_log_alpha(l4.x); la[1] = clamp_log_alpha(l4.y);
+          la[2] = clamp_log_alpha(l4.z); la[3] = clamp_log_alpha(l4.w);
+        }
+        run[0] += ok ? la[0] : 0.f;
+        run[1] += ok ? la[1] : 0.f;
+        run[2] += ok ? la[2] : 0.f;
+        run[3] += ok ? la[3] : 0.f;
 #pragma unroll
         for (int x = 0; x < 4; ++x) g[i][x] = run[x];
         cr.kraw[i] = ok ? *reinterpret_cast<const uint2*>(sm + kRawK + sw128_offset(C, r, 8 * lane))
@@ -459,6 +491,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         cr.qraw[i] = (kOut && ok)
                          ? *reinterpret_cast<const uint2*>(sm + kRawQ + sw128_offset(C, r, 8 * lane))
                          : make_uint2(0u, 0u);
+        if (FUSED) {  // token r's q and k over the warp: L2-normalise, round to bf16
+          cr.kraw[i] = l2norm_bf16x4(cr.kraw[i]);
+          if (kOut) cr.qraw[i] = l2norm_bf16x4(cr.qraw[i]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_raw);  // this warp is done with the raw tiles
@@ -918,7 +954,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool FUSED>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
@@ -927,7 +963,9 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
     const bool ok = make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
                     make_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
                     make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
-                    make_map(&maps.la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32);
+                    (FUSED ? make_map(&maps.la, a.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64)
+                           : make_map(&maps.la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T,
+                                      a.H, 32));
     if (!ok) return cudaErrorInvalidValue;
   }
   // The register split inside the kernel assumes the launch allocation; a
@@ -936,18 +974,18 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   static int launch_regs = -1;
   if (launch_regs < 0) {
     cudaFuncAttributes fa;
-    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE>);
+    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED>);
     if (ea != cudaSuccess) return ea;
     launch_regs = fa.numRegs;
   }
   if (static_cast<uint32_t>(launch_regs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   dim3 grid(a.plan.capacity, a.H, MODE == kModeSummary ? 2 : 1);
   prof_begin(s, name);
-  prefill_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
+  prefill_tc_kernel<MODE, FUSED><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
   return cudaGetLastError();
 }
@@ -955,11 +993,13 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
 }  // namespace
 
 cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s) {
-  return launch_tc<kModeSummary>(a, s, "kda_prefill_summary");
+  return a.fused ? launch_tc<kModeSummary, true>(a, s, "kda_prefill_summary")
+                 : launch_tc<kModeSummary, false>(a, s, "kda_prefill_summary");
 }
 
 cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s) {
-  return launch_tc<kModeReplay>(a, s, "kda_prefill_replay");
+  return a.fused ? launch_tc<kModeReplay, true>(a, s, "kda_prefill_replay")
+                 : launch_tc<kModeReplay, false>(a, s, "kda_prefill_replay");
 }
 
 }  // namespace kda

@@ -182,6 +182,42 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * kda_chunk_fwd_fused, kda_decode_step_fused -- the same layer with the input
+ * preparation done on load, so a caller passes projections straight through.
+ *
+ * The pages bound the forget gate's log-decay below at -5 by changing the
+ * decay curve itself (lecture "Inside Kimi K3: Architecture of an Open
+ * Frontier Model", sequence paragraph; orkas.ai close read, section "A lower
+ * bound that deleted a GPU code path": the activation is bounded below).
+ * These entry points take that curve's input, a gate logit x per key
+ * channel, and form log alpha = -5 * sigmoid(x) = -5 / (1 + e^-x) in fp32,
+ * then apply the same clamp to [-5, 0].  q and k arrive unnormalised; each
+ * (token, head) vector is scaled to unit L2 norm over its dk channels,
+ * x / max(||x||_2, 1e-12), in fp32 and rounded to bf16 (nearest even) before
+ * use -- the same values a caller would pass to kda_chunk_fwd /
+ * kda_decode_step after normalising itself.
+ *
+ * Arguments, layouts, ownership and errors are those of kda_chunk_fwd
+ * (respectively kda_decode_step), except:
+ *   q_raw, k_raw  bf16 [T, H, dk]   (decode: [N, H, dk])  unnormalised
+ *   gate          bf16 [T, H, dk]   (decode: [N, H, dk])  logits, in place of
+ *                                   log_alpha
+ * Prefill reads 2 * dk fewer bytes per token and head than kda_chunk_fwd
+ * (bf16 gate instead of f32 log_alpha).
+ */
+kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, const void *v,
+                               const void *gate, const float *beta,
+                               const float *S0, const int32_t *cu_seqlens,
+                               void *out, float *S_final, int64_t total_tokens,
+                               int32_t n_seqs, int32_t n_heads, int32_t dk,
+                               int32_t dv, void *stream);
+kda_status kda_decode_step_fused(const void *q_raw, const void *k_raw, const void *v,
+                                 const void *gate, const float *beta,
+                                 float *S_inout, void *out, int32_t n_seqs,
+                                 int32_t n_heads, int32_t dk, int32_t dv,
+                                 void *stream);
+
+/*
  * kda_get_device_error -- synchronise `stream`, then return and clear the
  * device error word of the current device: KDA_OK, or KDA_ERR_DEVICE_INPUT
  * when a kernel rejected an input (kda_last_error_message() names it), or

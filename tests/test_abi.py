@@ -127,3 +127,28 @@ def test_decode_rejects_bad_arguments(lib):
 
 def test_build_targets_sm103a():
     assert "arch=compute_103a,code=sm_103a" in kb.ARCH_FLAGS
+
+
+def fused_prefill(lib, T=128, N=2, H=2, dk=64, dv=64, **over):
+    names = ["q", "k", "v", "gate", "beta", "S0", "cu_seqlens", "out", "S_final"]
+    p = {n: P(i) for i, n in enumerate(names)}
+    p["cu_seqlens"] = None
+    p.update(over)
+    return lib.kda_chunk_fwd_fused(*[p[n] for n in names], T, N, H, dk, dv, None)
+
+
+def test_fused_entry_points_validate_like_the_plain_ones(lib):
+    assert fused_prefill(lib, gate=None) == INVALID
+    assert b"gate is NULL" in lib.kda_last_error_message()
+    assert fused_prefill(lib, dk=96, dv=96) == UNSUPPORTED
+    assert fused_prefill(lib, gate=P(3, 8)) == INVALID    # misaligned
+    assert b"gate" in lib.kda_last_error_message()
+    # the gate is bf16: T*H*dk*2 = 32 KiB, so `out` 40 KiB past its start is clear of it
+    # but 24 KiB past it lands inside
+    assert fused_prefill(lib, T=128, H=2, dk=64, out=P(3, 24 * 1024)) == INVALID
+    assert b"out overlaps gate" in lib.kda_last_error_message()
+    assert fused_prefill(lib, T=0, N=0) == OK
+    args = [P(i) for i in range(7)]
+    assert lib.kda_decode_step_fused(*args[:5], None, args[6], 4, 2, 64, 64, None) == INVALID
+    assert lib.kda_decode_step_fused(*args, 4, 2, 32, 32, None) == UNSUPPORTED
+    assert lib.kda_decode_step_fused(*args, 0, 2, 64, 64, None) == OK
