@@ -137,20 +137,58 @@ __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
 __device__ __forceinline__ uint2 pack4_bf16(const float (&f)[4]) {
   return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
 }
-// Fused input preparation: one token's 128 channels, 4 per lane across the
-// warp, scaled to unit L2 norm (x / max(||x||, 1e-12)) and rounded to bf16.
-// Every lane of the warp must call it.
-__device__ __forceinline__ uint2 l2norm_bf16x4(uint2 raw) {
-  float f[4];
-  f[0] = __uint_as_float(raw.x << 16);
-  f[1] = __uint_as_float(raw.x & 0xffff0000u);
-  f[2] = __uint_as_float(raw.y << 16);
-  f[3] = __uint_as_float(raw.y & 0xffff0000u);
-  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
+// Fused input preparation.  The 8 vectors k_r, q_r of a warp's 4 tokens each
+// span the warp (4 channels per lane); each is scaled to unit L2 norm,
+// x / max(||x||, 1e-12), and rounded to bf16.  The 8 sums of squares are
+// reduced together: three exchange steps halve the set each time (4 + 2 + 1
+// shuffles), two more finish one sum per lane (vector 4 * bit4 + 2 * bit3 +
+// bit2 of the lane), and 8 shuffles from lanes 4j hand the scales back --
+// 17 shuffles instead of 40.  Every lane of the warp must call it.
+__device__ __forceinline__ void l2norm8_bf16(uint2 (&kr)[4], uint2 (&qr)[4], int lane) {
+  float f[8][4];
 #pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float sc = l2_scale(ss);
-  return make_uint2(pack_bf16x2(f[0] * sc, f[1] * sc), pack_bf16x2(f[2] * sc, f[3] * sc));
+  for (int i = 0; i < 4; ++i) {
+    const uint2 a = kr[i], b = qr[i];
+    f[i][0] = __uint_as_float(a.x << 16); f[i][1] = __uint_as_float(a.x & 0xffff0000u);
+    f[i][2] = __uint_as_float(a.y << 16); f[i][3] = __uint_as_float(a.y & 0xffff0000u);
+    f[4 + i][0] = __uint_as_float(b.x << 16); f[4 + i][1] = __uint_as_float(b.x & 0xffff0000u);
+    f[4 + i][2] = __uint_as_float(b.y << 16); f[4 + i][3] = __uint_as_float(b.y & 0xffff0000u);
+  }
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    v[j] = f[j][0] * f[j][0] + f[j][1] * f[j][1] + f[j][2] * f[j][2] + f[j][3] * f[j][3];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float w[4], x[2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float give = b4 ? v[j] : v[j + 4];
+    w[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, give, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float give = b3 ? w[j] : w[j + 2];
+    x[j] = (b3 ? w[j + 2] : w[j]) + __shfl_xor_sync(0xffffffffu, give, 8);
+  }
+  float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+  y += __shfl_xor_sync(0xffffffffu, y, 2);
+  y += __shfl_xor_sync(0xffffffffu, y, 1);
+  const float sc_own = fminf(rsqrtf(y), 1e12f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float sc = __shfl_sync(0xffffffffu, sc_own, 4 * j);
+    const uint2 o = make_uint2(pack_bf16x2(f[j][0] * sc, f[j][1] * sc),
+                               pack_bf16x2(f[j][2] * sc, f[j][3] * sc));
+    if (j < 4) kr[j] = o; else qr[j - 4] = o;
+  }
+}
+
+// Fused input preparation: log alpha = -5 sigmoid(x) from a gate logit (the
+// approximate exponential and reciprocal; e^-x = inf gives 0).
+__device__ __forceinline__ float gate_log_alpha_fast(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-x)));
+  return clamp_log_alpha(-5.0f * r);
 }
 
 __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
@@ -473,7 +511,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           float gf[4];
           unpack4(*reinterpret_cast<const uint2*>(sm + kRawL + sw128_offset(C, r, 8 * lane)), gf);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) la[x] = gate_log_alpha(gf[x]);
+          for (int x = 0; x < 4; ++x) la[x] = gate_log_alpha_fast(gf[x]);
         } else {
           const float4 l4 =
               *reinterpret_cast<const float4*>(sm + kRawL + sw128_offset(C, r, 16 * lane));
@@ -491,11 +529,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         cr.qraw[i] = (kOut && ok)
                          ? *reinterpret_cast<const uint2*>(sm + kRawQ + sw128_offset(C, r, 8 * lane))
                          : make_uint2(0u, 0u);
-        if (FUSED) {  // token r's q and k over the warp: L2-normalise, round to bf16
-          cr.kraw[i] = l2norm_bf16x4(cr.kraw[i]);
-          if (kOut) cr.qraw[i] = l2norm_bf16x4(cr.qraw[i]);
-        }
       }
+      if (FUSED) l2norm8_bf16(cr.kraw, cr.qraw, lane);  // q, k of the warp's 4 tokens
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_raw);  // this warp is done with the raw tiles
       *reinterpret_cast<float4*>(sTot + warp * 128 + 4 * lane) =
