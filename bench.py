@@ -353,6 +353,29 @@ def time_decode(kb, dec, steps_per_run, warmup, runs=3):
     return start.elapsed_time(stop) / (runs * steps_per_run), kernels
 
 
+def time_decode_tokens(kb, dec, calls, warmup):
+    """kda_decode_tokens with all of a call's tokens committed: [N, K, ...]
+    inputs resident on the device, `calls` timed calls in a row."""
+    f = lambda t: t.transpose(0, 1).contiguous().cuda()
+    q, k, v, la, b = f(dec.q), f(dec.k), f(dec.v), f(dec.log_alpha), f(dec.beta)
+    S = dec.S.cuda()
+    out = torch.empty(tuple(v.shape), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        kb.kda_decode_tokens(q, k, v, la, b, S, None, out, stream=stream)
+    torch.cuda.synchronize()
+    kb.profile_read()
+    kb.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(calls):
+        kb.kda_decode_tokens(q, k, v, la, b, S, None, out, stream=stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    kb.profile_enable(False)
+    return start.elapsed_time(stop) / calls, kb.profile_read()
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def cpu_sample(p, n_seqs, max_tokens=None):
@@ -539,6 +562,23 @@ def main():
                          "kernel": "kda_decode_step", "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": dbytes}}
         del dec
+        # several tokens per call (speculative drafts): 8 tokens of each of the
+        # same 256 x 32 sequence-heads, all committed
+        K = 8
+        decK = kin.make_decode(256, 32, 128, steps=K, seed=4)
+        tms, tk = time_decode_tokens(kb, decK, 20, args.warmup)
+        n_sh = 256 * 32
+        tbytes = n_sh * (8 * 128 * 128 + K * (12 * 128 + 4))
+        tn, tt = tk["kda_decode_step"]
+        t_gbs = tbytes / (tt / tn * 1e-3) / 1e9
+        line["decode_tokens"] = {
+            "workload": f"batched decode 256 seqs H32 d128, {K} tokens per call, all committed",
+            "value": 256 * K / (tms * 1e-3), "unit": "tokens/s", "ms_per_call": tms,
+            "roofline": {"bound": "hbm", "achieved": t_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": t_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "kda_decode_step", "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": tbytes}}
+        del decK
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -106,6 +106,8 @@ def load():
             lib.kda_chunk_fwd_fused.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
             lib.kda_decode_step_fused.restype = ctypes.c_int
             lib.kda_decode_step_fused.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
+            lib.kda_decode_tokens.restype = ctypes.c_int
+            lib.kda_decode_tokens.argtypes = [vp] * 8 + [i32, i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int
             lib.kda_get_device_error.argtypes = [vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -257,3 +259,27 @@ def profile_read():
     n = load().kda_profile_read(buf, 32)
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
             for i in range(n)}
+
+
+def kda_decode_tokens(q, k, v, log_alpha, beta, S_inout, commit=None, out=None, *, stream=None):
+    """K tokens per sequence from the state ``S_inout`` [N, H, dk, dv] f32.
+
+    q, k: bf16 [N, K, H, dk]; v bf16 [N, K, H, dv]; log_alpha f32 [N, K, H, dk];
+    beta f32 [N, K, H]; commit: int32 [N] (CUDA) or None (commit all K).
+    Returns out bf16 [N, K, H, dv]; ``S_inout`` holds the state after the
+    committed tokens of each sequence.
+    """
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S_inout, torch.float32, "S_inout"),
+                        (commit, torch.int32, "commit")):
+        _require(t, dt, name)
+    if out is None:
+        out = torch.empty((N, K, H, dv), dtype=torch.bfloat16, device=q.device)
+    _require(out, torch.bfloat16, "out")
+    _check(load().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                    _ptr(S_inout), _ptr(out), _ptr(commit), N, K, H, dk, dv,
+                                    _stream(stream)))
+    return out

@@ -305,13 +305,14 @@ extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const vo
                         n_seqs, n_heads, dk, dv, segment_tokens, false, stream);
 }
 
-// fused as in chunk_fwd_impl
+// fused as in chunk_fwd_impl.  K tokens per sequence; commit: device [N] or null.
 static kda_status decode_impl(const void* q, const void* k, const void* v, const void* log_alpha,
-                              const float* beta, float* S_inout, void* out, int32_t N, int32_t H,
-                              int32_t dk, int32_t dv, bool fused, void* stream) {
+                              const float* beta, float* S_inout, void* out, const int32_t* commit,
+                              int32_t N, int32_t K, int32_t H, int32_t dk, int32_t dv, bool fused,
+                              void* stream) {
   const char* la_name = fused ? "gate" : "log_alpha";
-  if (N < 0 || H <= 0)
-    return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs=%d n_heads=%d", N, H);
+  if (N < 0 || H <= 0 || K <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs=%d n_tokens=%d n_heads=%d", N, K, H);
   kda_status st = check_head_dims(dk, dv);
   if (st != KDA_OK) return st;
   if (N == 0) return KDA_OK;
@@ -322,23 +323,37 @@ static kda_status decode_impl(const void* q, const void* k, const void* v, const
     if (!r.p) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", r.n);
     if (misaligned(r.p)) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", r.n);
   }
+  if (misaligned(commit)) return fail(KDA_ERR_INVALID_ARGUMENT, "commit is not 16-byte aligned");
   const int64_t nh = static_cast<int64_t>(N) * H;
-  Range r_out = range_of("out", out, nh * dv * 2);
-  Range others[] = {range_of("q", q, nh * dk * 2), range_of("k", k, nh * dk * 2),
-                    range_of("v", v, nh * dv * 2),
-                    range_of(la_name, log_alpha, nh * dk * (fused ? 2 : 4)),
-                    range_of("beta", beta, nh * 4), range_of("S_inout", S_inout, nh * dk * dv * 4)};
+  const int64_t th = nh * K;  // (token, head) rows
+  Range r_out = range_of("out", out, th * dv * 2);
+  Range others[] = {range_of("q", q, th * dk * 2), range_of("k", k, th * dk * 2),
+                    range_of("v", v, th * dv * 2),
+                    range_of(la_name, log_alpha, th * dk * (fused ? 2 : 4)),
+                    range_of("beta", beta, th * 4),
+                    range_of("commit", commit, commit ? static_cast<int64_t>(N) * 4 : 0),
+                    range_of("S_inout", S_inout, nh * dk * dv * 4)};
   for (auto& r : others)
     if (overlaps(r_out, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps %s", r.name);
-  for (int i = 0; i < 5; ++i)
-    if (overlaps(others[5], others[i]))
+  for (int i = 0; i < 6; ++i)
+    if (overlaps(others[6], others[i]))
       return fail(KDA_ERR_INVALID_ARGUMENT, "S_inout overlaps %s", others[i].name);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(
-      static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
-      static_cast<const uint16_t*>(v), fused ? nullptr : static_cast<const float*>(log_alpha),
-      fused ? static_cast<const uint16_t*>(log_alpha) : nullptr, beta, S_inout,
-      static_cast<uint16_t*>(out), N, H, dk, dv, s);
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != KDA_OK) return st;
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.log_alpha = fused ? nullptr : static_cast<const float*>(log_alpha);
+  a.gate = fused ? static_cast<const uint16_t*>(log_alpha) : nullptr;
+  a.beta = beta;
+  a.S = S_inout;
+  a.out = static_cast<uint16_t*>(out);
+  a.commit = commit;
+  a.N = N; a.K = K; a.H = H; a.dk = dk; a.dv = dv;
+  a.err = dev->err;
+  cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KDA_OK;
 }
@@ -347,14 +362,25 @@ extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* 
                                       const float* log_alpha, const float* beta,
                                       float* S_inout, void* out, int32_t N, int32_t H,
                                       int32_t dk, int32_t dv, void* stream) {
-  return decode_impl(q, k, v, log_alpha, beta, S_inout, out, N, H, dk, dv, false, stream);
+  return decode_impl(q, k, v, log_alpha, beta, S_inout, out, nullptr, N, 1, H, dk, dv, false,
+                     stream);
 }
 
 extern "C" kda_status kda_decode_step_fused(const void* q_raw, const void* k_raw, const void* v,
                                             const void* gate, const float* beta, float* S_inout,
                                             void* out, int32_t N, int32_t H, int32_t dk,
                                             int32_t dv, void* stream) {
-  return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, N, H, dk, dv, true, stream);
+  return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, nullptr, N, 1, H, dk, dv, true,
+                     stream);
+}
+
+extern "C" kda_status kda_decode_tokens(const void* q, const void* k, const void* v,
+                                        const float* log_alpha, const float* beta,
+                                        float* S_inout, void* out, const int32_t* commit,
+                                        int32_t N, int32_t K, int32_t H, int32_t dk, int32_t dv,
+                                        void* stream) {
+  return decode_impl(q, k, v, log_alpha, beta, S_inout, out, commit, N, K, H, dk, dv, false,
+                     stream);
 }
 
 extern "C" kda_status kda_get_device_error(void* stream) {
@@ -376,6 +402,7 @@ extern "C" kda_status kda_get_device_error(void* stream) {
     msg += "cu_seqlens is malformed (cu[0] != 0, decreasing, or cu[N] != total_tokens); ";
   if (word & kDevErrCapacity) msg += "segment plan exceeded its workspace; ";
   if (word & kDevErrTimeout) msg += "a prefill kernel timed out waiting for its tensor-core work; ";
+  if (word & kDevErrCommit) msg += "a decode commit count is outside [0, n_tokens]; ";
   return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
 }
 

@@ -19,6 +19,7 @@ enum DeviceError : int {
   kDevErrCuSeqlens = 1,      // cu_seqlens malformed
   kDevErrCapacity = 2,       // more segments than the workspace holds
   kDevErrTimeout = 4,        // a kernel gave up waiting on its own async copies / MMAs
+  kDevErrCommit = 8,         // a decode commit count outside [0, tokens per call]
 };
 
 // One segment of one sequence: tokens [t0, t1) (global indices).
@@ -83,12 +84,20 @@ cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s);
 
 // ---- decode (kda_decode.cu)
-// gate != null selects the fused input preparation (raw q, k; bf16 gate logits)
-cudaError_t launch_decode(const uint16_t* q, const uint16_t* k,
-                          const uint16_t* v, const float* log_alpha,
-                          const uint16_t* gate, const float* beta, float* S,
-                          uint16_t* out, int32_t N, int32_t H, int32_t dk,
-                          int32_t dv, cudaStream_t s);
+struct DecodeArgs {
+  const uint16_t* q;        // bf16 [N*K, H, dk]
+  const uint16_t* k;
+  const uint16_t* v;        // bf16 [N*K, H, dv]
+  const float* log_alpha;   // f32 [N*K, H, dk]; null when gate is given
+  const uint16_t* gate;     // bf16 [N*K, H, dk] logits (fused preparation) or null
+  const float* beta;        // f32 [N*K, H]
+  float* S;                 // f32 [N, H, dk, dv], updated in place
+  uint16_t* out;            // bf16 [N*K, H, dv]
+  const int32_t* commit;    // [N] tokens to commit per sequence, or null (all K)
+  int32_t N, K, H, dk, dv;
+  int* err;                 // device error word
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // bf16 helpers usable from device code without cuda_bf16.h conversions.
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {

@@ -182,6 +182,43 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * kda_decode_tokens -- several tokens per sequence in one call, with a commit
+ * count: the form speculative decoding needs.
+ *
+ * For each sequence n, the n_tokens tokens t = 0 .. n_tokens-1 are applied in
+ * order starting from S_inout[n], exactly as n_tokens kda_decode_step calls
+ * would.  out receives every token's output.  S_inout[n] is then overwritten
+ * with the state after the first commit[n] tokens only: commit[n] = 0 leaves
+ * it untouched, commit = NULL commits all n_tokens.  The state is updated in
+ * place and cannot be rolled back (orkas.ai close read, section "The bill
+ * comes due in the serving stack"). So a draft of k tokens is verified with
+ * a call that commits nothing. A second call over the same cached inputs
+ * then commits the accepted prefix: the state is rebuilt from the inputs,
+ * not undone.  The state is read once and written at most once per call, so
+ * a call costs about one decode step of memory traffic for all its tokens.
+ *
+ * Tensors (N = n_seqs, K = n_tokens; token t of sequence n is row n*K + t):
+ *   q, k        bf16 [N*K, H, dk]   read
+ *   v           bf16 [N*K, H, dv]   read
+ *   log_alpha   f32  [N*K, H, dk]   read; clamped to [-5, 0]
+ *   beta        f32  [N*K, H]       read
+ *   S_inout     f32  [N, H, dk, dv] read; written as described
+ *   out         bf16 [N*K, H, dv]   written
+ *   commit      i32  [N] on the device, each in [0, K], or NULL.  A value
+ *               outside [0, K] is reported through kda_get_device_error
+ *               (KDA_ERR_DEVICE_INPUT); that sequence's out and state are
+ *               then left unwritten.
+ * n_tokens >= 1; n_tokens = 1 with commit = NULL is kda_decode_step.  Other
+ * rules as kda_decode_step (commit must not overlap S_inout or out).
+ * Allocates nothing.
+ */
+kda_status kda_decode_tokens(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta,
+                             float *S_inout, void *out, const int32_t *commit,
+                             int32_t n_seqs, int32_t n_tokens, int32_t n_heads,
+                             int32_t dk, int32_t dv, void *stream);
+
+/*
  * kda_chunk_fwd_fused, kda_decode_step_fused -- the same layer with the input
  * preparation done on load, so a caller passes projections straight through.
  *

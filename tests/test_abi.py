@@ -152,3 +152,13 @@ def test_fused_entry_points_validate_like_the_plain_ones(lib):
     assert lib.kda_decode_step_fused(*args[:5], None, args[6], 4, 2, 64, 64, None) == INVALID
     assert lib.kda_decode_step_fused(*args, 4, 2, 32, 32, None) == UNSUPPORTED
     assert lib.kda_decode_step_fused(*args, 0, 2, 64, 64, None) == OK
+
+
+def test_decode_tokens_validates_arguments(lib):
+    a = [P(i) for i in range(8)]
+    assert lib.kda_decode_tokens(*a, 4, 0, 2, 64, 64, None) == INVALID        # no tokens
+    assert lib.kda_decode_tokens(*a[:7], P(7, 4), 4, 3, 2, 64, 64, None) == INVALID  # commit misaligned
+    assert b"commit" in lib.kda_last_error_message()
+    assert lib.kda_decode_tokens(*a[:6], P(7), P(7), 4, 3, 2, 64, 64, None) == INVALID  # out over commit
+    assert lib.kda_decode_tokens(*a, 4, 3, 2, 96, 96, None) == UNSUPPORTED
+    assert lib.kda_decode_tokens(*a, 0, 3, 2, 64, 64, None) == OK

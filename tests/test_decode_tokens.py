@@ -1,0 +1,91 @@
+"""kda_decode_tokens: K tokens per sequence per call with a commit count
+(speculative decoding's verify / commit), against the fp64 oracle and
+against K single decode steps."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_48_gb300 import binding as kb
+from gated_delta_rule_48_gb300 import inputs as kin
+from kda_testlib import check_out, check_state
+
+pytestmark = pytest.mark.gpu
+
+
+def _seq_major(d):
+    """make_decode's [steps, N, ...] tensors as [N, steps, ...] (sequence n's tokens together)."""
+    f = lambda t: t.transpose(0, 1).contiguous()
+    return f(d.q), f(d.k), f(d.v), f(d.log_alpha), f(d.beta)
+
+
+def _oracle(q, k, v, la, b, S, commit):
+    """Outputs of all K tokens from S, and each sequence's state after its first commit[n]."""
+    N, K = q.shape[:2]
+    flat = lambda t: t.reshape((N * K,) + tuple(t.shape[2:]))
+    bits = lambda t: kin.bf16_bits(flat(t))
+    cu = np.arange(N + 1) * K
+    out, _ = oracle.forward(bits(q), bits(k), bits(v), flat(la).numpy(), flat(b).numpy(),
+                            S.numpy(), cu)
+    # committed prefixes: a packed batch of the first commit[n] tokens of each sequence
+    keep = np.concatenate([np.arange(n * K, n * K + c) for n, c in enumerate(commit)]).astype(int)
+    cu_c = np.concatenate([[0], np.cumsum(commit)])
+    _, S_c = oracle.forward(bits(q)[keep], bits(k)[keep], bits(v)[keep], flat(la).numpy()[keep],
+                            flat(b).numpy()[keep], S.numpy(), cu_c)
+    return out.reshape((N, K) + out.shape[1:]), S_c
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_tokens_commit_all_and_partial(d):
+    dec = kin.make_decode(48, 4, d, steps=8, seed=41)
+    q, k, v, la, b = _seq_major(dec)
+    rng = np.random.default_rng(41)
+    for commit in (np.full(48, 8), rng.integers(0, 9, size=48)):
+        S = dec.S.cuda()
+        out = kb.kda_decode_tokens(q.cuda(), k.cuda(), v.cuda(), la.cuda(), b.cuda(), S,
+                                   torch.from_numpy(commit.astype(np.int32)).cuda())
+        assert kb.kda_get_device_error() == 0
+        ref_o, ref_S = _oracle(q, k, v, la, b, dec.S, commit)
+        check_out(out.float().cpu().numpy(), ref_o)
+        check_state(S.cpu().numpy(), ref_S)
+        # commit 0 leaves the state bit-identical
+        zero = commit == 0
+        np.testing.assert_array_equal(S.cpu().numpy()[zero], dec.S.numpy()[zero])
+
+
+def test_decode_tokens_equals_single_steps_bitwise():
+    """Verify (commit 0), then commit the accepted prefix: the result is exactly
+    the state after that many kda_decode_step calls."""
+    dec = kin.make_decode(32, 4, 128, steps=6, seed=42)
+    q, k, v, la, b = (t.cuda() for t in _seq_major(dec))
+    accept = np.array([6, 0, 3, 1] * 8, dtype=np.int32)
+    S = dec.S.cuda()
+    out_v = kb.kda_decode_tokens(q, k, v, la, b, S, torch.zeros(32, dtype=torch.int32, device="cuda"))
+    assert torch.equal(S, dec.S.cuda())                       # verify wrote no state
+    out_c = kb.kda_decode_tokens(q, k, v, la, b, S, torch.from_numpy(accept).cuda())
+    assert torch.equal(out_v, out_c)                          # outputs do not depend on commit
+    S1 = dec.S.cuda()                 # state of the sequential single steps
+    S_ref = dec.S.cuda().clone()      # expected committed state (accept 0: the start)
+    for t in range(6):
+        o = kb.kda_decode_step(q[:, t].contiguous(), k[:, t].contiguous(), v[:, t].contiguous(),
+                               la[:, t].contiguous(), b[:, t].contiguous(), S1)
+        assert torch.equal(o, out_c[:, t])
+        done = torch.from_numpy(accept == t + 1).cuda()
+        S_ref[done] = S1[done]
+    assert torch.equal(S, S_ref)
+
+
+def test_decode_tokens_rejects_commit_out_of_range():
+    dec = kin.make_decode(4, 2, 64, steps=3, seed=43)
+    q, k, v, la, b = (t.cuda() for t in _seq_major(dec))
+    S = dec.S.cuda()
+    out = torch.full((4, 3, 2, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    commit = torch.tensor([3, 4, 0, -1], dtype=torch.int32, device="cuda")
+    kb.kda_decode_tokens(q, k, v, la, b, S, commit, out=out)
+    assert kb.kda_get_device_error() == 5  # KDA_ERR_DEVICE_INPUT
+    assert b"commit" in kb.load().kda_last_error_message()
+    # the rejected sequences (1 and 3) are untouched, the others ran
+    assert torch.equal(S[1], dec.S[1].cuda()) and torch.equal(S[3], dec.S[3].cuda())
+    assert torch.isnan(out[1].float()).all() and torch.isnan(out[3].float()).all()
+    assert not torch.isnan(out[0].float()).any() and not torch.isnan(out[2].float()).any()
+    assert not torch.equal(S[0], dec.S[0].cuda())
