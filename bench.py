@@ -45,6 +45,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fused", action="store_true")
+    ap.add_argument("--no-checkpoints", action="store_true")
     return ap.parse_args()
 
 
@@ -283,6 +284,36 @@ def time_prefill_fused(kb, r, steps, warmup):
     torch.cuda.synchronize()
     kb.profile_enable(False)
     return start.elapsed_time(stop) / steps, kb.profile_read()
+
+
+def time_prefill_checkpoints(kb, p, interval, steps, warmup):
+    """kda_chunk_fwd_checkpoints on device-resident inputs; returns (ms per step,
+    checkpoints per step)."""
+    d = _device_inputs(p)
+    cu = d["cu_seqlens"]
+    if cu is None:
+        cu = torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda()
+    lens = np.diff(p.cu_seqlens)
+    n_ck = int(np.sum(lens // interval))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return kb.kda_chunk_fwd_checkpoints(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                            d["S0"], cu, interval=interval,
+                                            max_checkpoints=n_ck, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    if kb.kda_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / steps, n_ck
 
 
 def time_prefill_e2e(kb, p, steps, warmup):
@@ -545,6 +576,17 @@ def main():
                          "algorithmic_bytes_per_launch": fbytes}}
         line["gpu_launches_fused"] = sum(n for n, _ in fk.values())
         del r
+
+    if not args.no_checkpoints:
+        # the same prefill, also emitting the state every 1024 tokens of each sequence
+        cms, n_ck = time_prefill_checkpoints(kb, p, 1024, max(3, min(args.steps, 50)),
+                                             args.warmup)
+        line["checkpoints"] = {
+            "workload": workload_config(p, args.workload)["workload"]
+                        + ", state checkpoint every 1024 tokens",
+            "value": p.total_T / (cms * 1e-3) / 1e6, "unit": "Mtok/s", "ms_per_step": cms,
+            "checkpoints_per_step": n_ck * p.H,
+            "checkpoint_bytes_per_step": n_ck * p.H * d * d * 4}
 
     if not args.no_decode:
         dec = kin.decode_workload(steps=args.decode_steps)

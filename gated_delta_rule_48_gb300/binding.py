@@ -106,6 +106,8 @@ def load():
             lib.kda_chunk_fwd_fused.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, vp]
             lib.kda_decode_step_fused.restype = ctypes.c_int
             lib.kda_decode_step_fused.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
+            lib.kda_chunk_fwd_checkpoints.restype = ctypes.c_int
+            lib.kda_chunk_fwd_checkpoints.argtypes = ([vp] * 9 + [i64, i32, i32, i32, i32, i64, vp, i64, vp])
             lib.kda_decode_tokens.restype = ctypes.c_int
             lib.kda_decode_tokens.argtypes = [vp] * 8 + [i32, i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int
@@ -283,3 +285,30 @@ def kda_decode_tokens(q, k, v, log_alpha, beta, S_inout, commit=None, out=None, 
                                     _ptr(S_inout), _ptr(out), _ptr(commit), N, K, H, dk, dv,
                                     _stream(stream)))
     return out
+
+
+def kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, interval,
+                              max_checkpoints, n_seqs=None, stream=None):
+    """Prefill that also returns the state after every ``interval`` tokens of each
+    sequence (see include/kda.h).  Returns (out, S_final, checkpoints), checkpoints
+    f32 [max_checkpoints, H, dk, dv] packed sequence by sequence."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.shape[0] - 1
+    elif n_seqs is None:
+        n_seqs = 1
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S0, torch.float32, "S0"),
+                        (cu_seqlens, torch.int32, "cu_seqlens")):
+        _require(t, dt, name)
+    out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
+    S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    ck = torch.empty((max(int(max_checkpoints), 1), H, dk, dv), dtype=torch.float32,
+                     device=q.device)[:int(max_checkpoints)]
+    _check(load().kda_chunk_fwd_checkpoints(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+        _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv, int(interval),
+        _ptr(ck) if int(max_checkpoints) > 0 else None, int(max_checkpoints), _stream(stream)))
+    return out, S_final, ck

@@ -170,6 +170,7 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                                  const float* S0, const int32_t* cu_seqlens, void* out,
                                  float* S_final, int64_t T, int32_t N, int32_t H,
                                  int32_t dk, int32_t dv, int64_t segment_tokens, bool fused,
+                                 int64_t ckpt_interval, float* ckpt, int64_t ckpt_max,
                                  void* stream_v) {
   const char* la_name = fused ? "gate" : "log_alpha";
   // ---- host-side checks: nothing is launched unless all pass
@@ -186,6 +187,15 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   if (segment_tokens > 0 && segment_tokens % kChunk != 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "segment_tokens=%lld is not a multiple of %d",
                 (long long)segment_tokens, kChunk);
+  if (ckpt_interval != 0) {
+    if (ckpt_interval < 0 || ckpt_interval % kChunk != 0 || ckpt_interval > 0x7fffffffLL)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint interval=%lld is not a positive multiple of %d",
+                  (long long)ckpt_interval, kChunk);
+    if (ckpt_max < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "max_checkpoints=%lld", (long long)ckpt_max);
+    if (ckpt_max > 0 && !ckpt) return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoints is NULL");
+    if (misaligned(ckpt))
+      return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoints is not 16-byte aligned");
+  }
   if (T > 0) {
     const struct { const void* p; const char* n; } req[] = {
         {q, "q"}, {k, "k"}, {v, "v"}, {log_alpha, la_name}, {beta, "beta"}, {out, "out"}};
@@ -205,6 +215,12 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                 range_of("cu_seqlens", cu_seqlens, cu_seqlens ? (N + 1) * 4 : 0)};
   Range r_out = range_of("out", out, T > 0 ? v_bytes : 0);
   Range r_sf = range_of("S_final", S_final, S_final ? s_bytes : 0);
+  const int64_t ck_bytes = (ckpt_interval > 0 && ckpt) ? ckpt_max * H * dk * dv * 4 : 0;
+  Range r_ck = range_of("checkpoints", ckpt, ck_bytes);
+  for (const Range& r : in)
+    if (overlaps(r_ck, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoints overlap %s", r.name);
+  if (overlaps(r_ck, r_out) || overlaps(r_ck, r_sf))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoints overlap out or S_final");
   for (int i = 0; i < 7; ++i) {
     const Range& r = in[i];
     if (overlaps(r_out, r)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps %s", r.name);
@@ -237,7 +253,10 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   size_t it_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)(dv + dk) : 0;
   size_t off_es = align_up(off_it + it_bytes);
   size_t es_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)dv : 0;
-  size_t ws_bytes = align_up(off_es + es_bytes);
+  const bool want_ckpt = ckpt_interval > 0;  // the planner counts (and flags an overflow) even if max = 0
+  size_t off_ck = align_up(off_es + es_bytes);
+  size_t ck_base_bytes = want_ckpt ? sizeof(int64_t) * (size_t)N : 0;
+  size_t ws_bytes = align_up(off_ck + ck_base_bytes);
 
   char* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s);
@@ -260,6 +279,12 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.plan.segs = reinterpret_cast<Segment*>(ws + off_segs);
   a.plan.n_segs = reinterpret_cast<int32_t*>(ws + off_nseg);
   a.plan.capacity = capacity;
+  if (want_ckpt) {
+    a.plan.ckpt_base = reinterpret_cast<int64_t*>(ws + off_ck);
+    a.plan.ckpt_interval = ckpt_interval;
+    a.plan.ckpt_max = ckpt_max;
+    a.ckpt = ckpt_max > 0 ? ckpt : nullptr;
+  }
   a.err = dev->err;
 
   kda_status result = KDA_OK;
@@ -283,7 +308,7 @@ extern "C" kda_status kda_chunk_fwd(const void* q, const void* k, const void* v,
                                     float* S_final, int64_t total_tokens, int32_t n_seqs,
                                     int32_t n_heads, int32_t dk, int32_t dv, void* stream) {
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
-                        n_seqs, n_heads, dk, dv, 0, false, stream);
+                        n_seqs, n_heads, dk, dv, 0, false, 0, nullptr, 0, stream);
 }
 
 extern "C" kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, const void* v,
@@ -292,7 +317,7 @@ extern "C" kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, 
                                           int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
                                           int32_t dk, int32_t dv, void* stream) {
   return chunk_fwd_impl(q_raw, k_raw, v, gate, beta, S0, cu_seqlens, out, S_final, total_tokens,
-                        n_seqs, n_heads, dk, dv, 0, true, stream);
+                        n_seqs, n_heads, dk, dv, 0, true, 0, nullptr, 0, stream);
 }
 
 extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const void* v,
@@ -302,7 +327,23 @@ extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const vo
                                           int32_t n_seqs, int32_t n_heads, int32_t dk,
                                           int32_t dv, int64_t segment_tokens, void* stream) {
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
-                        n_seqs, n_heads, dk, dv, segment_tokens, false, stream);
+                        n_seqs, n_heads, dk, dv, segment_tokens, false, 0, nullptr, 0,
+                        stream);
+}
+
+extern "C" kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v,
+                                                const float* log_alpha, const float* beta,
+                                                const float* S0, const int32_t* cu_seqlens,
+                                                void* out, float* S_final, int64_t total_tokens,
+                                                int32_t n_seqs, int32_t n_heads, int32_t dk,
+                                                int32_t dv, int64_t interval, float* checkpoints,
+                                                int64_t max_checkpoints, void* stream) {
+  if (interval <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint interval=%lld is not a positive multiple of %d",
+                (long long)interval, kChunk);
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
+                        n_seqs, n_heads, dk, dv, 0, false, interval, checkpoints, max_checkpoints,
+                        stream);
 }
 
 // fused as in chunk_fwd_impl.  K tokens per sequence; commit: device [N] or null.
@@ -403,6 +444,8 @@ extern "C" kda_status kda_get_device_error(void* stream) {
   if (word & kDevErrCapacity) msg += "segment plan exceeded its workspace; ";
   if (word & kDevErrTimeout) msg += "a prefill kernel timed out waiting for its tensor-core work; ";
   if (word & kDevErrCommit) msg += "a decode commit count is outside [0, n_tokens]; ";
+  if (word & kDevErrCheckpoints)
+    msg += "the sequences have more checkpoints than max_checkpoints (the excess was dropped); ";
   return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
 }
 

@@ -20,6 +20,7 @@ enum DeviceError : int {
   kDevErrCapacity = 2,       // more segments than the workspace holds
   kDevErrTimeout = 4,        // a kernel gave up waiting on its own async copies / MMAs
   kDevErrCommit = 8,         // a decode commit count outside [0, tokens per call]
+  kDevErrCheckpoints = 16,   // more prefill checkpoints than the caller's buffer holds
 };
 
 // One segment of one sequence: tokens [t0, t1) (global indices).
@@ -36,6 +37,12 @@ struct Plan {
   Segment* segs;       // [capacity]
   int32_t* n_segs;     // [1] number of valid segments
   int32_t capacity;
+  // prefill state checkpoints (ckpt_interval > 0): sequence n's checkpoint j
+  // (the state after its first j * ckpt_interval tokens, j >= 1) goes to slot
+  // ckpt_base[n] + j - 1 of the caller's buffer, slots >= ckpt_max dropped
+  int64_t* ckpt_base = nullptr;  // [N], written by the planner
+  int64_t ckpt_interval = 0;
+  int64_t ckpt_max = 0;
 };
 
 // Problem description shared by the prefill kernels.
@@ -59,6 +66,7 @@ struct PrefillArgs {
   // L2-normalised on load; log alpha comes from the bf16 gate logits
   int fused = 0;
   const uint16_t* gate = nullptr;  // bf16 [T, H, dk] when fused
+  float* ckpt = nullptr;           // f32 [ckpt_max, H, dk, dv] state checkpoints, or null
 };
 
 // ---- error reporting shared by the entry points (kda_api.cu)

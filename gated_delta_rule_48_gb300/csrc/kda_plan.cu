@@ -30,8 +30,11 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
   __shared__ int s_bad;
   __shared__ int32_t s_scan[kPlanThreads];
   __shared__ int32_t s_base;
+  __shared__ int64_t s_cscan[kPlanThreads];  // checkpoint counts
+  __shared__ int64_t s_cbase;
   const int tid = threadIdx.x;
-  if (tid == 0) { s_bad = 0; s_base = 0; }
+  const int64_t CI = plan.ckpt_interval;
+  if (tid == 0) { s_bad = 0; s_base = 0; s_cbase = 0; }
   __syncthreads();
 
   // 1. validate cu_seqlens
@@ -58,14 +61,19 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
       cnt = 1;
       if (L > 0 && len > L) cnt = static_cast<int32_t>((len + L - 1) / L);
     }
+    const int64_t ccnt = (n < N && CI > 0) ? len / CI : 0;  // checkpoints of this sequence
     s_scan[tid] = cnt;
+    s_cscan[tid] = ccnt;
     __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {  // Hillis-Steele inclusive scan
+    for (int off = 1; off < kPlanThreads; off <<= 1) {  // Hillis-Steele inclusive scans
       int32_t add = tid >= off ? s_scan[tid - off] : 0;
+      int64_t cadd = tid >= off ? s_cscan[tid - off] : 0;
       __syncthreads();
       s_scan[tid] += add;
+      s_cscan[tid] += cadd;
       __syncthreads();
     }
+    if (n < N && CI > 0) plan.ckpt_base[n] = s_cbase + s_cscan[tid] - ccnt;
     const int32_t first = s_base + s_scan[tid] - cnt;
     if (n < N) {
       for (int32_t j = 0; j < cnt; ++j) {
@@ -82,9 +90,10 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
       }
     }
     __syncthreads();
-    if (tid == kPlanThreads - 1) s_base += s_scan[tid];
+    if (tid == kPlanThreads - 1) { s_base += s_scan[tid]; s_cbase += s_cscan[tid]; }
     __syncthreads();
   }
+  if (tid == 0 && CI > 0 && s_cbase > plan.ckpt_max) atomicOr(err, kDevErrCheckpoints);
   if (tid == 0) {
     if (s_bad) {
       atomicOr(err, kDevErrCapacity);

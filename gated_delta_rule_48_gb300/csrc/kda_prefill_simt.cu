@@ -86,6 +86,10 @@ prefill_simt_kernel(PrefillArgs a) {
     sm.S[i] = s0;
   }
 
+  // State checkpoints (replay): tokens of the sequence before this segment
+  const int64_t ckpt_ci = (MODE == 1 && a.ckpt) ? a.plan.ckpt_interval : 0;
+  const int64_t seq_t0 = ckpt_ci > 0 ? a.plan.segs[sg.first].t0 : 0;
+
   for (int64_t c0 = sg.t0; c0 < sg.t1; c0 += C) {
     const int valid = sg.t1 - c0 < C ? static_cast<int>(sg.t1 - c0) : C;
     __syncthreads();
@@ -207,6 +211,14 @@ prefill_simt_kernel(PrefillArgs a) {
       float acc = __expf(sm.glast[c]) * sm.S[i];
       for (int r = 0; r < C; ++r) acc += sm.w[r * LD + c] * sm.v[r * NB + j];
       sm.S[i] = acc;
+      if (ckpt_ci > 0) {  // the state after this chunk, if the sequence has a checkpoint here
+        const int64_t pos = c0 + valid - seq_t0;
+        if (pos % ckpt_ci == 0) {
+          const int64_t slot = a.plan.ckpt_base[sg.seq] + pos / ckpt_ci - 1;
+          if (slot < a.plan.ckpt_max)
+            a.ckpt[((slot * H + h) * D + c) * static_cast<int64_t>(DV) + col0 + j] = acc;
+        }
+      }
     }
   }
   __syncthreads();

@@ -351,7 +351,9 @@ __device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, in
   }
 }
 
-template <int MODE, bool FUSED>
+// CKPT (replay only): write the state checkpoints the plan asks for; a separate
+// instantiation, so the plain replay keeps its register budget.
+template <int MODE, bool FUSED, bool CKPT>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -652,6 +654,18 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
   };
 
+  // S^T (TMEM) -> dst[c * ld + j] = S[c][j] (row = key channel), f32; worker warps.
+  auto store_state = [&](float* dst, int64_t ld) {
+    const int j = 32 * quad + lane;
+#pragma unroll
+    for (int cc = 0; cc < 32; cc += 16) {
+      uint32_t sv[16];
+      tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+    }
+  };
   // ================= control warps: issue the MMA groups once their operands are ready.
   // Issuing a tcgen05.mma costs the issuing thread ~100 cycles, far more than
   // the tensor pipe needs for these shapes, so the two independent MMA chains
@@ -918,6 +932,27 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       }
       wait_done(3, n);
       worker_sync();
+      if (CKPT) {  // the state after this chunk, if the sequence has a checkpoint here
+        // tokens of the sequence up to this chunk's end (< 2^31: TMA coordinates are 32-bit)
+        const int32_t ci = static_cast<int32_t>(a.plan.ckpt_interval);
+        const int32_t pos = static_cast<int32_t>(sg.t0 - a.plan.segs[sg.first].t0) +
+                            static_cast<int32_t>(n) * C + chunk_valid(n);
+        if (pos % ci == 0) {
+          const int64_t slot = a.plan.ckpt_base[sg.seq] + pos / ci - 1;
+          if (slot < a.plan.ckpt_max) {  // 8 columns at a time: few live registers mid-loop
+            float* dst = a.ckpt + (slot * H + h) * D * D;
+            const int j = 32 * quad + lane;
+#pragma unroll 1
+            for (int cc = 0; cc < 32; cc += 8) {
+              uint32_t sv[16];
+              tmem_ld8(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 8; ++x) dst[(32 * part + cc + x) * D + j] = __uint_as_float(sv[x]);
+            }
+          }
+        }
+      }
     }
 
     if (kOut && n_chunks > 0 && !*s_abort) write_out(n_chunks - 1);
@@ -932,17 +967,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         ld = 2 * D;  // increment | transition record
         dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D) + (ident ? D : 0);
       }
-      if (dst) {
-        const int j = 32 * quad + lane;
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
-          uint32_t sv[16];
-          tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
-        }
-      }
+      if (dst) store_state(dst, ld);
     }
   }  // worker warps
   tc_fence_before();
@@ -989,7 +1014,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool FUSED>
+template <int MODE, bool FUSED, bool CKPT>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
@@ -1009,18 +1034,18 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   static int launch_regs = -1;
   if (launch_regs < 0) {
     cudaFuncAttributes fa;
-    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED>);
+    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED, CKPT>);
     if (ea != cudaSuccess) return ea;
     launch_regs = fa.numRegs;
   }
   if (static_cast<uint32_t>(launch_regs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED, CKPT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   dim3 grid(a.plan.capacity, a.H, MODE == kModeSummary ? 2 : 1);
   prof_begin(s, name);
-  prefill_tc_kernel<MODE, FUSED><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
+  prefill_tc_kernel<MODE, FUSED, CKPT><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
   return cudaGetLastError();
 }
@@ -1028,13 +1053,16 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
 }  // namespace
 
 cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s) {
-  return a.fused ? launch_tc<kModeSummary, true>(a, s, "kda_prefill_summary")
-                 : launch_tc<kModeSummary, false>(a, s, "kda_prefill_summary");
+  return a.fused ? launch_tc<kModeSummary, true, false>(a, s, "kda_prefill_summary")
+                 : launch_tc<kModeSummary, false, false>(a, s, "kda_prefill_summary");
 }
 
 cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s) {
-  return a.fused ? launch_tc<kModeReplay, true>(a, s, "kda_prefill_replay")
-                 : launch_tc<kModeReplay, false>(a, s, "kda_prefill_replay");
+  if (a.ckpt)
+    return a.fused ? launch_tc<kModeReplay, true, true>(a, s, "kda_prefill_replay")
+                   : launch_tc<kModeReplay, false, true>(a, s, "kda_prefill_replay");
+  return a.fused ? launch_tc<kModeReplay, true, false>(a, s, "kda_prefill_replay")
+                 : launch_tc<kModeReplay, false, false>(a, s, "kda_prefill_replay");
 }
 
 }  // namespace kda

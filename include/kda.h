@@ -182,6 +182,43 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * kda_chunk_fwd_checkpoints -- kda_chunk_fwd that also emits the state at
+ * regular token boundaries of every sequence, for a prefix cache.
+ *
+ * A fixed-size state at a token boundary is all a later call needs to
+ * continue from that prefix (orkas.ai close read, section "The bill comes
+ * due in the serving stack": to reuse a prefix, the recurrent state is
+ * checkpointed at a sparse subset of the token boundaries the cache hashes,
+ * e.g. every 1024 tokens when it hashes every 512).  For sequence n of length len_n and
+ * each j = 1 .. floor(len_n / interval), the state after the sequence's first
+ * j * interval tokens is written, f32 [dk][dv] per head (the layout of
+ * S_final), to
+ *     checkpoints[c_n + j - 1, h],   c_n = sum over m < n of floor(len_m / interval),
+ * so the checkpoints are packed sequence by sequence in token order.  A
+ * sequence whose length is a multiple of interval gets its final state as
+ * its last checkpoint too.
+ *
+ *   interval        > 0, a multiple of 64
+ *   checkpoints     f32 [max_checkpoints, H, dk, dv], written; must not
+ *                   overlap any other argument (may be NULL if
+ *                   max_checkpoints = 0)
+ *   max_checkpoints >= 0.  If the sequences have more checkpoints, the
+ *                   excess is dropped and kda_get_device_error reports
+ *                   KDA_ERR_DEVICE_INPUT; out and S_final are still written.
+ * Everything else as kda_chunk_fwd (including the automatic split of long
+ * sequences: checkpoints come from the replay, which starts every segment
+ * from its exact entry state).
+ */
+kda_status kda_chunk_fwd_checkpoints(const void *q, const void *k, const void *v,
+                                     const float *log_alpha, const float *beta,
+                                     const float *S0, const int32_t *cu_seqlens,
+                                     void *out, float *S_final,
+                                     int64_t total_tokens, int32_t n_seqs,
+                                     int32_t n_heads, int32_t dk, int32_t dv,
+                                     int64_t interval, float *checkpoints,
+                                     int64_t max_checkpoints, void *stream);
+
+/*
  * kda_decode_tokens -- several tokens per sequence in one call, with a commit
  * count: the form speculative decoding needs.
  *

@@ -162,3 +162,21 @@ def test_decode_tokens_validates_arguments(lib):
     assert lib.kda_decode_tokens(*a[:6], P(7), P(7), 4, 3, 2, 64, 64, None) == INVALID  # out over commit
     assert lib.kda_decode_tokens(*a, 4, 3, 2, 96, 96, None) == UNSUPPORTED
     assert lib.kda_decode_tokens(*a, 0, 3, 2, 64, 64, None) == OK
+
+
+def test_checkpoints_validate_arguments(lib):
+    names = ["q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"]
+    p = [P(i) for i in range(9)]
+    p[6] = None
+
+    def call(interval=128, ck=P(9), mx=4, T=256, N=2):
+        return lib.kda_chunk_fwd_checkpoints(*p, T, N, 2, 64, 64, interval, ck, mx, None)
+
+    assert call(interval=0) == INVALID
+    assert call(interval=100) == INVALID                 # not a multiple of 64
+    assert b"interval" in lib.kda_last_error_message()
+    assert call(ck=None) == INVALID
+    assert call(ck=P(9, 8)) == INVALID                   # misaligned
+    assert call(ck=P(7, 64)) == INVALID                  # inside out
+    assert b"checkpoints overlap" in lib.kda_last_error_message()
+    assert call(T=0, N=0) == OK
