@@ -108,6 +108,8 @@ def load():
             lib.kda_decode_step_fused.argtypes = [vp] * 7 + [i32, i32, i32, i32, vp]
             lib.kda_chunk_fwd_checkpoints.restype = ctypes.c_int
             lib.kda_chunk_fwd_checkpoints.argtypes = ([vp] * 9 + [i64, i32, i32, i32, i32, i64, vp, i64, vp])
+            lib.kda_chunk_fwd_host.restype = ctypes.c_int
+            lib.kda_chunk_fwd_host.argtypes = [vp] * 8 + [i64, i32, i32, i32, i32, i64, vp]
             lib.kda_decode_tokens.restype = ctypes.c_int
             lib.kda_decode_tokens.argtypes = [vp] * 8 + [i32, i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int
@@ -312,3 +314,25 @@ def kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None
         _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv, int(interval),
         _ptr(ck) if int(max_checkpoints) > 0 else None, int(max_checkpoints), _stream(stream)))
     return out, S_final, ck
+
+
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, S0, out, S_final, *, n_seqs, slice_tokens=0,
+                       stream=None):
+    """Prefill of a uniform batch held in HOST tensors (pin them for overlap).
+
+    q, k, v, log_alpha, beta, out, S0 / S_final as in :func:`kda_chunk_fwd`, but CPU
+    tensors; out and S_final are written once ``stream`` is synchronised."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S0, torch.float32, "S0"),
+                        (out, torch.bfloat16, "out"), (S_final, torch.float32, "S_final")):
+        if t is None:
+            continue
+        if t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise KdaError(1, f"{name} must be a contiguous CPU {dt} tensor")
+    _check(load().kda_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                     _ptr(S0), _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv,
+                                     int(slice_tokens), _stream(stream)))
+    return out, S_final

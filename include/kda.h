@@ -182,6 +182,36 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * kda_chunk_fwd_host -- kda_chunk_fwd for a uniform batch whose tensors are
+ * in HOST memory (pinned memory makes the copies asynchronous).
+ *
+ * Nothing on the pages; it serves callers whose inputs and outputs live on
+ * the host.  The batch is processed in time slices of `slice_tokens` tokens
+ * per sequence (0 = 512; otherwise a multiple of 64).  Internal streams
+ * overlap three things: the host-to-device copy of slice i+1, the prefill
+ * of slice i, and the device-to-host copy of slice i-1.  The state stays
+ * on the device and carries from slice to slice (the in-place continuation
+ * of kda_chunk_fwd), so the results equal one kda_chunk_fwd call on the whole
+ * batch up to rounding.
+ *
+ *   q, k, v, log_alpha, beta, out   HOST pointers, layouts of kda_chunk_fwd
+ *                                   with cu_seqlens = NULL (N sequences of
+ *                                   total_tokens / N tokens each)
+ *   S0, S_final                     HOST pointers or NULL, as kda_chunk_fwd
+ * The call is ordered on `stream` like every entry point and returns before
+ * the work is done: the host buffers must stay valid, and out / S_final must
+ * not be read, until `stream` has been synchronised.  Device staging (two
+ * slices of inputs and outputs, plus the state) is allocated stream-ordered
+ * on `stream` and released at the end.
+ */
+kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const float *S0, void *out, float *S_final,
+                              int64_t total_tokens, int32_t n_seqs,
+                              int32_t n_heads, int32_t dk, int32_t dv,
+                              int64_t slice_tokens, void *stream);
+
+/*
  * kda_chunk_fwd_checkpoints -- kda_chunk_fwd that also emits the state at
  * regular token boundaries of every sequence, for a prefix cache.
  *

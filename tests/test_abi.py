@@ -180,3 +180,12 @@ def test_checkpoints_validate_arguments(lib):
     assert call(ck=P(7, 64)) == INVALID                  # inside out
     assert b"checkpoints overlap" in lib.kda_last_error_message()
     assert call(T=0, N=0) == OK
+
+
+def test_host_api_validates_arguments(lib):
+    a = [P(i) for i in range(8)]
+    assert lib.kda_chunk_fwd_host(*a, 100, 3, 2, 64, 64, 0, None) == INVALID   # not a multiple
+    assert lib.kda_chunk_fwd_host(*a, 96, 3, 2, 64, 64, 100, None) == INVALID  # slice not x64
+    assert lib.kda_chunk_fwd_host(*a, 96, 3, 2, 96, 96, 0, None) == UNSUPPORTED
+    assert lib.kda_chunk_fwd_host(None, *a[1:], 96, 3, 2, 64, 64, 0, None) == INVALID
+    assert lib.kda_chunk_fwd_host(*a, 0, 0, 2, 64, 64, 0, None) == OK
