@@ -259,7 +259,14 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   size_t ws_bytes = align_up(off_ck + ck_base_bytes);
 
   char* ws = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s);
+  // Stream capture turns the allocation into a graph memory node, which takes
+  // the default pool; otherwise the library's own pool keeps workspace cached.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  e = cap == cudaStreamCaptureStatusNone
+          ? cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s)
+          : cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
 
   PrefillArgs a;

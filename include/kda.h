@@ -27,7 +27,10 @@
  *   returns KDA_ERR_UNSUPPORTED.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every call is asynchronous with respect to the host and ordered
- *   on `stream`; calls on different streams may run concurrently.
+ *   on `stream`; calls on different streams may run concurrently.  The device
+ *   entry points never synchronise the host and allocate only stream-ordered,
+ *   so they can be captured into a CUDA graph (make one uncaptured call per
+ *   device first: it creates the library's per-device state).
  * - The caller owns every buffer.  The library keeps no caller pointer after
  *   a call returns.  Inputs are never written.
  * - Errors found on the host (null pointer, bad size, misalignment,
