@@ -99,9 +99,10 @@ typedef enum {
  * A uniform batch [B, T_b, H, d] is passed as T = B * T_b, N = B,
  * cu_seqlens = NULL.  T = 0 or N = 0 is a valid no-op (S_final = S0).
  *
- * Memory: allocates a temporary workspace stream-ordered on `stream`
- * (cudaMallocAsync / cudaFreeAsync) when sequences are split; size grows
- * with (N + T / segment) * H * dk * (dv + dk) * 4 bytes.
+ * Memory: allocates a temporary workspace stream-ordered on `stream` and
+ * frees it there: the segment plan (32 bytes per segment) and, when sequences
+ * are split, (N + T / segment) * H * dk * (2 dv + dk) * 4 bytes of segment
+ * summaries and entry states.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta,
