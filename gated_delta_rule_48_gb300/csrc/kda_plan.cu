@@ -104,25 +104,47 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
   }
 }
 
-// Entry states of split sequences: one CTA per (sequence, head, column block
-// of kScanCols state columns).  Sequential over the sequence's segments.
-constexpr int kScanCols = 32;
+// Entry states of split sequences, S_in(j+1) = M_j S_in(j) + B_j: one CTA per
+// (sequence, head, block of kScanCols state columns), sequential over the
+// sequence's segments.  The whole M_j (D x D f32, from the summary records)
+// is staged in shared memory by cp.async, the next segment's copy in flight
+// while the current one is used; rows are padded by 4 floats so the threads
+// reading 4 different rows hit different banks.
+constexpr int kScanCols = 8;
 constexpr int kScanThreads = 256;
+
+template <int D>
+struct ScanSmem {
+  static constexpr int LD = D + 4;
+  float M[2][D * LD];
+  float S[D * kScanCols];
+};
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kScanThreads)
 segment_scan_kernel(PrefillArgs a) {
+  extern __shared__ __align__(16) unsigned char scan_smem[];
+  ScanSmem<D>& sm = *reinterpret_cast<ScanSmem<D>*>(scan_smem);
+  constexpr int LD = ScanSmem<D>::LD;
+  constexpr int RPT = D * kScanCols / kScanThreads;  // output rows per thread (4 or 2)
   const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kScanCols;
   const int32_t n_segs = *a.plan.n_segs;
-  // find this sequence's first segment (segments are ordered by sequence)
   __shared__ int32_t s_first, s_count;
-  __shared__ float sS[D][kScanCols];
-  __shared__ float sM[32][D + 1];  // 32 rows of M_j at a time
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_first = -1;
     s_count = 0;
-    // binary search over segments for seq == n, index == 0
+    // binary search over segments for seq == n, index == 0 (segments are ordered by sequence)
     int lo = 0, hi = n_segs;
     while (lo < hi) {
       int mid = (lo + hi) >> 1;
@@ -136,45 +158,49 @@ segment_scan_kernel(PrefillArgs a) {
   __syncthreads();
   if (s_first < 0 || s_count <= 1) return;
   const int W = a.dv + D;  // width of the B | M record
+  auto rec_of = [&](int64_t seg) {
+    return a.incr_trans + (seg * a.H + h) * static_cast<int64_t>(D) * W;
+  };
+  auto stage_M = [&](int buf, const float* rec) {  // M_j -> sm.M[buf], 16 bytes per copy
+    for (int i = tid; i < D * (D / 4); i += kScanThreads) {
+      const int c = i / (D / 4), m4 = i % (D / 4);
+      cp_async16(&sm.M[buf][c * LD + 4 * m4], rec + static_cast<int64_t>(c) * W + a.dv + 4 * m4);
+    }
+    cp_async_commit();
+  };
+  stage_M(0, rec_of(s_first));
   for (int i = tid; i < D * kScanCols; i += kScanThreads) {
     const int c = i / kScanCols, j = i % kScanCols;
-    sS[c][j] = a.S0 ? a.S0[((static_cast<int64_t>(n) * a.H + h) * D + c) * a.dv + col0 + j] : 0.f;
+    sm.S[i] = a.S0 ? a.S0[((static_cast<int64_t>(n) * a.H + h) * D + c) * a.dv + col0 + j] : 0.f;
   }
-  __syncthreads();
+  const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + 32 r
   for (int sgi = 0; sgi + 1 < s_count; ++sgi) {
     const int64_t seg = s_first + sgi;
-    const float* rec = a.incr_trans + (seg * a.H + h) * static_cast<int64_t>(D) * W;
-    // each thread owns outputs (c, j) with j = tid % 32, c = tid / 32 + 8 r
-    float acc[D / 8];
+    const float* rec = rec_of(seg);
+    float acc[RPT];
 #pragma unroll
-    for (int r = 0; r < D / 8; ++r) {
-      const int c = tid / kScanCols + 8 * r;
-      acc[r] = rec[static_cast<int64_t>(c) * W + col0 + (tid % kScanCols)];  // B_j
-    }
-    for (int m0 = 0; m0 < D; m0 += 32) {
-      // stage M_j[:, m0:m0+32] transposed as sM[m][c]
-      __syncthreads();
-      for (int i = tid; i < D * 32; i += kScanThreads) {
-        const int c = i / 32, m = i % 32;
-        sM[m][c] = rec[static_cast<int64_t>(c) * W + a.dv + m0 + m];
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < D / 8; ++r) {
-        const int c = tid / kScanCols + 8 * r;
-        float s = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < 32; ++m) s += sM[m][c] * sS[m0 + m][tid % kScanCols];
-        acc[r] += s;
-      }
+    for (int r = 0; r < RPT; ++r) acc[r] = rec[static_cast<int64_t>(c0 + 32 * r) * W + col0 + j];  // B_j
+    if (sgi + 2 < s_count) {  // stage the next transition while this one is used
+      stage_M((sgi + 1) & 1, rec_of(seg + 1));
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const float* Mb = sm.M[sgi & 1];
+#pragma unroll 4
+    for (int m = 0; m < D; ++m) {
+      const float sv = sm.S[m * kScanCols + j];
 #pragma unroll
-    for (int r = 0; r < D / 8; ++r) {
-      const int c = tid / kScanCols + 8 * r;
-      sS[c][tid % kScanCols] = acc[r];
+      for (int r = 0; r < RPT; ++r) acc[r] = fmaf(Mb[(c0 + 32 * r) * LD + m], sv, acc[r]);
+    }
+    __syncthreads();  // every thread has read S_in(j) and this M buffer
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const int c = c0 + 32 * r;
+      sm.S[c * kScanCols + j] = acc[r];
       a.entry_state[((seg + 1) * a.H + h) * static_cast<int64_t>(D) * a.dv +
-                    static_cast<int64_t>(c) * a.dv + col0 + (tid % kScanCols)] = acc[r];
+                    static_cast<int64_t>(c) * a.dv + col0 + j] = acc[r];
     }
     __syncthreads();
   }
@@ -193,12 +219,20 @@ cudaError_t launch_plan(const int32_t* cu_seqlens, int64_t T, int32_t N, int64_t
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s) {
   dim3 grid(a.N, a.H, a.dv / kScanCols);
   prof_begin(s, "kda_segment_scan");
-  if (a.dk == 128)
-    segment_scan_kernel<128><<<grid, kScanThreads, 0, s>>>(a);
-  else
-    segment_scan_kernel<64><<<grid, kScanThreads, 0, s>>>(a);
+  cudaError_t e;
+  if (a.dk == 128) {
+    e = cudaFuncSetAttribute(segment_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(ScanSmem<128>)));
+    if (e == cudaSuccess)
+      segment_scan_kernel<128><<<grid, kScanThreads, sizeof(ScanSmem<128>), s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(segment_scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(ScanSmem<64>)));
+    if (e == cudaSuccess)
+      segment_scan_kernel<64><<<grid, kScanThreads, sizeof(ScanSmem<64>), s>>>(a);
+  }
   prof_end(s, "kda_segment_scan");
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kda
