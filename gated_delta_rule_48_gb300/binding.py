@@ -110,6 +110,8 @@ def load():
             lib.kda_chunk_fwd_checkpoints.argtypes = ([vp] * 9 + [i64, i32, i32, i32, i32, i64, vp, i64, vp])
             lib.kda_chunk_fwd_host.restype = ctypes.c_int
             lib.kda_chunk_fwd_host.argtypes = [vp] * 8 + [i64, i32, i32, i32, i32, i64, vp]
+            lib.kda_decode_tokens_fused.restype = ctypes.c_int
+            lib.kda_decode_tokens_fused.argtypes = [vp] * 8 + [i32, i32, i32, i32, i32, vp]
             lib.kda_decode_tokens.restype = ctypes.c_int
             lib.kda_decode_tokens.argtypes = [vp] * 8 + [i32, i32, i32, i32, i32, vp]
             lib.kda_get_device_error.restype = ctypes.c_int
@@ -336,3 +338,22 @@ def kda_chunk_fwd_host(q, k, v, log_alpha, beta, S0, out, S_final, *, n_seqs, sl
                                      _ptr(S0), _ptr(out), _ptr(S_final), T, n_seqs, H, dk, dv,
                                      int(slice_tokens), _stream(stream)))
     return out, S_final
+
+
+def kda_decode_tokens_fused(q_raw, k_raw, v, gate, beta, S_inout, commit=None, out=None, *,
+                            stream=None):
+    """:func:`kda_decode_tokens` with raw q, k and bf16 gate logits [N, K, H, dk]."""
+    N, K, H, dk = q_raw.shape
+    dv = v.shape[-1]
+    for t, dt, name in ((q_raw, torch.bfloat16, "q_raw"), (k_raw, torch.bfloat16, "k_raw"),
+                        (v, torch.bfloat16, "v"), (gate, torch.bfloat16, "gate"),
+                        (beta, torch.float32, "beta"), (S_inout, torch.float32, "S_inout"),
+                        (commit, torch.int32, "commit")):
+        _require(t, dt, name)
+    if out is None:
+        out = torch.empty((N, K, H, dv), dtype=torch.bfloat16, device=q_raw.device)
+    _require(out, torch.bfloat16, "out")
+    _check(load().kda_decode_tokens_fused(_ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(gate),
+                                          _ptr(beta), _ptr(S_inout), _ptr(out), _ptr(commit),
+                                          N, K, H, dk, dv, _stream(stream)))
+    return out

@@ -422,6 +422,15 @@ extern "C" kda_status kda_decode_step_fused(const void* q_raw, const void* k_raw
                      stream);
 }
 
+extern "C" kda_status kda_decode_tokens_fused(const void* q_raw, const void* k_raw,
+                                              const void* v, const void* gate,
+                                              const float* beta, float* S_inout, void* out,
+                                              const int32_t* commit, int32_t N, int32_t K,
+                                              int32_t H, int32_t dk, int32_t dv, void* stream) {
+  return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, commit, N, K, H, dk, dv, true,
+                     stream);
+}
+
 extern "C" kda_status kda_decode_tokens(const void* q, const void* k, const void* v,
                                         const float* log_alpha, const float* beta,
                                         float* S_inout, void* out, const int32_t* commit,

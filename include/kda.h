@@ -290,7 +290,8 @@ kda_status kda_decode_tokens(const void *q, const void *k, const void *v,
                              int32_t dk, int32_t dv, void *stream);
 
 /*
- * kda_chunk_fwd_fused, kda_decode_step_fused -- the same layer with the input
+ * kda_chunk_fwd_fused, kda_decode_step_fused, kda_decode_tokens_fused -- the
+ * same layer with the input
  * preparation done on load, so a caller passes projections straight through.
  *
  * The pages bound the forget gate's log-decay below at -5 by changing the
@@ -306,7 +307,7 @@ kda_status kda_decode_tokens(const void *q, const void *k, const void *v,
  * kda_decode_step after normalising itself.
  *
  * Arguments, layouts, ownership and errors are those of kda_chunk_fwd
- * (respectively kda_decode_step), except:
+ * (respectively kda_decode_step, kda_decode_tokens), except:
  *   q_raw, k_raw  bf16 [T, H, dk]   (decode: [N, H, dk])  unnormalised
  *   gate          bf16 [T, H, dk]   (decode: [N, H, dk])  logits, in place of
  *                                   log_alpha
@@ -319,6 +320,11 @@ kda_status kda_chunk_fwd_fused(const void *q_raw, const void *k_raw, const void 
                                void *out, float *S_final, int64_t total_tokens,
                                int32_t n_seqs, int32_t n_heads, int32_t dk,
                                int32_t dv, void *stream);
+kda_status kda_decode_tokens_fused(const void *q_raw, const void *k_raw, const void *v,
+                                   const void *gate, const float *beta,
+                                   float *S_inout, void *out, const int32_t *commit,
+                                   int32_t n_seqs, int32_t n_tokens, int32_t n_heads,
+                                   int32_t dk, int32_t dv, void *stream);
 kda_status kda_decode_step_fused(const void *q_raw, const void *k_raw, const void *v,
                                  const void *gate, const float *beta,
                                  float *S_inout, void *out, int32_t n_seqs,
