@@ -242,17 +242,22 @@ def time_prefill(kb, p, steps, warmup, world):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with ClockSampler(torch.cuda.current_device()) as clocks:
         start.record(stream)
-        for _ in range(steps):
+        for i in range(steps):
+            marks[i].record(stream)
             step()
+        marks[steps].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     kb.profile_enable(False)
     kernels = kb.profile_read()
     ms = start.elapsed_time(stop) / steps
-    return ms, kernels, clocks.summary()
+    per = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(steps))
+    stats = {"median": per[len(per) // 2], "min": per[0], "max": per[-1]}
+    return ms, kernels, clocks.summary(), stats
 
 
 def time_prefill_fused(kb, r, steps, warmup):
@@ -543,7 +548,7 @@ def main():
     alg_bytes = prefill_bytes(th, sh, d, p.S0 is not None)
     alg_flops = prefill_flops(th, d)
 
-    ms, kernels, clocks = time_prefill(kb, p, args.steps, args.warmup, world)
+    ms, kernels, clocks, step_stats = time_prefill(kb, p, args.steps, args.warmup, world)
     ms = max_over_ranks(ms, world)
     tokens_all = sum_over_ranks(p.total_T, world)
     value = tokens_all / (ms * 1e-3) / 1e6  # Mtok/s over all ranks
@@ -569,7 +574,15 @@ def main():
                      "algorithmic_bytes_per_launch": per_launch_bytes},
         "tensor": {"tflops": tflops, "bf16_peak": peaks["bf16_tflops"],
                    "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-                   "algorithmic_flops_per_step": alg_flops, "peak_source": peak_src},
+                   # attainable = min(tensor peak, arithmetic intensity x HBM bandwidth)
+                   "attainable_tflops": min(peaks["bf16_tflops"],
+                                            alg_flops / alg_bytes * peaks["hbm_gbs"] / 1e3),
+                   "frac_of_attainable": tflops / min(peaks["bf16_tflops"],
+                                                      alg_flops / alg_bytes * peaks["hbm_gbs"] / 1e3),
+                   "algorithmic_flops_per_step": alg_flops,
+                   "dense_tile_flops_per_step": th * (6 * d * d + 10 * CHUNK * d),
+                   "peak_source": peak_src},
+        "step_ms": step_stats,
         "kernels": {k: {"launches": n, "avg_ms": t / n} for k, (n, t) in kernels.items()},
         "gpu_launches": launches,
         "clocks": clocks,
@@ -626,7 +639,8 @@ def main():
         kern_gbs = dbytes / (dt / dn * 1e-3) / 1e9
         line["decode"] = {
             "workload": kin.WORKLOADS[4], "value": dbytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
-            "ms_per_step": dms, "tokens_per_s": n_sh / dec.q.shape[2] / (dms * 1e-3),
+            "ms_per_step": dms, "ms_per_64_steps": 64 * dms,
+            "tokens_per_s": n_sh / dec.q.shape[2] / (dms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": kern_gbs / peaks["hbm_gbs"],
                          "traffic": recorded_traffic("kda_decode_step", "kda_decode.cu"),
@@ -662,6 +676,13 @@ def main():
             "kind": "oracle", "cpu": cpu_model(), "seconds": sec,
             "sample": f"first {min(p.n_seqs, 4)} sequences of the workload ({sample['tokens']} "
                       f"tokens x {p.H} heads), fp64 token-by-token recurrence"}
+        # the same oracle on one thread, on the tiny workload (token-heads per second)
+        p0 = kin.workload(0)
+        s0 = cpu_sample(p0, p0.n_seqs)
+        sec0 = min(time_oracle(s0, 1) for _ in range(3))
+        line["cpu_baseline"]["single_thread"] = {
+            "value": s0["tokens"] * p0.H / sec0, "unit": "token-heads/s", "cores": 1,
+            "sample": kin.WORKLOADS[0]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
