@@ -843,7 +843,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           }
         }
       }
-      worker_sync();
+      // The inverse reads only the key rows (odd lane quadrants, A_kk); its
+      // first step runs on warps 0 and 1.  Those nine warps meet here; the
+      // query-row warps (A_qk) join at the inverse's next barrier, so their
+      // longer read-out overlaps the diagonal blocks.
+      if (warp == 0 || (warp & 1)) asm volatile("bar.sync 2, 288;" ::: "memory");
       ut_transform(sAkk, reinterpret_cast<float*>(R + kRXs), reinterpret_cast<const float*>(KP),
                    sBeta, R, tid);
       signal_ready(1);  // T, k e^g, V ready for the WY products
