@@ -121,3 +121,68 @@ def test_fused_decode_matches_fused_prefill():
     out_p, S_p = prep.forward_fused(*[pack(b) for b in bits], pack(d.beta.numpy()), d.S.numpy(), cu)
     np.testing.assert_allclose(S, S_p, rtol=0, atol=0)
     np.testing.assert_allclose(np.swapaxes(out, 0, 1).reshape(out_p.shape), out_p, rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- planted mistakes
+# Each case replaces one step of oracle.prep with a plausible slip and runs the
+# pins above against the modified module: at least one must fail.
+import types
+
+
+def _pins(mod):
+    saved = {}
+    failed = 0
+    pins = [test_round_bf16_matches_torch_on_float32_values, test_round_bf16_ties_go_to_even,
+            test_gate_curve_is_minus_five_logistic, test_normalise_unit_norm_per_token_head,
+            test_prepare_scale_invariant_and_unit_vectors_unchanged,
+            test_normalise_floor_zero_and_tiny_vectors]
+    for name in ("round_bf16", "gate_log_alpha", "l2_normalise", "prepare"):
+        saved[name] = getattr(prep, name)
+        setattr(prep, name, getattr(mod, name))
+    try:
+        for pin in pins:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failed += 1
+    finally:
+        for name, fn in saved.items():
+            setattr(prep, name, fn)
+    return failed
+
+
+def _mutant(**overrides):
+    mod = types.SimpleNamespace(round_bf16=prep.round_bf16, gate_log_alpha=prep.gate_log_alpha,
+                                l2_normalise=prep.l2_normalise)
+    for k, v in overrides.items():
+        setattr(mod, k, v)
+
+    def prepare(q_raw_bits, k_raw_bits, gate_bits):
+        q = mod.round_bf16(mod.l2_normalise(prep.bf16_bits_to_f64(q_raw_bits)))
+        k = mod.round_bf16(mod.l2_normalise(prep.bf16_bits_to_f64(k_raw_bits)))
+        return q, k, mod.gate_log_alpha(prep.bf16_bits_to_f64(gate_bits))
+    mod.prepare = prepare
+    return mod
+
+
+MUTANTS = {
+    "gate sign flipped": dict(gate_log_alpha=lambda g: -5.0 / (1.0 + np.exp(np.asarray(g, float)))),
+    "gate scale 4 instead of 5": dict(gate_log_alpha=lambda g: -4.0 / (1.0 + np.exp(-np.asarray(g, float)))),
+    "normalised over heads": dict(l2_normalise=lambda x: np.asarray(x, float) / np.maximum(
+        np.sqrt(np.sum(np.asarray(x, float) ** 2, axis=-2, keepdims=True)), 1e-12)),
+    "no floor on the norm": dict(l2_normalise=lambda x: np.asarray(x, float) / np.sqrt(
+        np.sum(np.asarray(x, float) ** 2, axis=-1, keepdims=True))),
+    "rounded by truncation": dict(round_bf16=lambda x: np.ldexp(np.trunc(np.ldexp(
+        np.frexp(np.asarray(x, float))[0], 8)), np.frexp(np.asarray(x, float))[1] - 8)),
+    "no rounding": dict(round_bf16=lambda x: np.asarray(x, float)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_each_planted_prep_mistake_fails_a_pin(name):
+    with np.errstate(all="ignore"):
+        assert _pins(_mutant(**MUTANTS[name])) >= 1, f"no pin caught: {name}"
+
+
+def test_unmodified_prep_passes_every_pin():
+    assert _pins(_mutant()) == 0
