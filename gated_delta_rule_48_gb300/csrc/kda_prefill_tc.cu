@@ -196,133 +196,182 @@ __device__ __forceinline__ uint4 pack4_tf32(const float (&f)[4]) {
                     f32_to_tf32_rn(f[3]));
 }
 
-// T[r][c] = f (= T'[r][c] beta_c) into the three operand copies of T: tf32
-// (rounded to nearest) [64][64] and the bf16 pair hi + lo, all 128-byte swizzled.
-__device__ __forceinline__ void put_T(unsigned char* __restrict__ R, int r, int c, float f) {
-  *reinterpret_cast<uint32_t*>(R + kRT + sw128_offset(C, r, 4 * c)) = f32_to_tf32_rn(f);
-  const __nv_bfloat16 hi = __float2bfloat16_rn(f);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(f - __bfloat162float(hi));
-  *reinterpret_cast<__nv_bfloat16*>(R + kRTh + sw128_offset(C, r, 2 * c)) = hi;
-  *reinterpret_cast<__nv_bfloat16*>(R + kRTl + sw128_offset(C, r, 2 * c)) = lo;
+// T[r][4j .. 4j+3] = f (already T'[r][c] beta_c) into the three operand copies
+// of T: tf32 (rounded to nearest) [64][64] and the bf16 pair hi + lo, all
+// 128-byte swizzled.  One 16-byte and two 8-byte stores.
+__device__ __forceinline__ void put_T4(unsigned char* __restrict__ R, int r, int j, float4 f) {
+  *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, r, 16 * j)) =
+      make_uint4(f32_to_tf32_rn(f.x), f32_to_tf32_rn(f.y), f32_to_tf32_rn(f.z), f32_to_tf32_rn(f.w));
+  const uint32_t h0 = pack_bf16x2(f.x, f.y), h1 = pack_bf16x2(f.z, f.w);
+  const uint32_t l0 = pack_bf16x2(f.x - __uint_as_float(h0 << 16), f.y - __uint_as_float(h0 & 0xffff0000u));
+  const uint32_t l1 = pack_bf16x2(f.z - __uint_as_float(h1 << 16), f.w - __uint_as_float(h1 & 0xffff0000u));
+  *reinterpret_cast<uint2*>(R + kRTh + sw128_offset(C, r, 8 * j)) = make_uint2(h0, h1);
+  *reinterpret_cast<uint2*>(R + kRTl + sw128_offset(C, r, 8 * j)) = make_uint2(l0, l1);
+}
+
+__device__ __forceinline__ float f4c(const float4& v, int u) {  // component u (unrolled: constant)
+  return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w;
 }
 
 // UT transform.  sA holds a strictly lower-triangular 64 x 64 matrix A (f32,
 // row stride kLdA, zero on and above the diagonal).  Computes
 // T' = (I + A)^{-1} (unit lower-triangular) by doubling and writes
-// T = T' Diag(beta) into its operand copies (put_T):
-//   1. the four 16 x 16 diagonal blocks, by column-oriented forward
-//      substitution in registers (one thread per column), in place;
-//   2. 16 -> 32: T'_{b+1,b} = -T'_{b+1,b+1} A_{b+1,b} T'_{bb} for b = 0, 2, in place;
-//   3. 32 -> 64: T'_(10) = -T'_(11) A_(10) T'_(00) on 32 x 32 halves, straight
-//      to T; the finished halves T'_(00), T'_(11) (and the zero T'_(01)) go to T
-//      meanwhile.
-// Xs is scratch for the intermediate products (32 x 36 floats); A10T holds
-// the transposed block A_(10) (A10T[i][r] = A[32 + r][i]).  4 barriers.
+// T = T' Diag(beta) into its operand copies (put_T4).  Blocks of 16: D_b is
+// the inverse of diagonal block b, subscripts (10), (00), (11) are 32 x 32
+// halves.
+//   warps 0, 1 (h = warp), with warp-level syncs only:
+//     1. D_2h and D_2h+1 by forward substitution (lane = block, column),
+//        in place; A is read 4 entries of a row per load;
+//     2. T'_ab = -D_a (A_ab D_b) for (a, b) = (2h + 1, 2h), in place: lane =
+//        (row, 8 columns), the product A_ab D_b through the scratch Xs;
+//   warps 2..15 meanwhile zero T'_(01) in the copies.
+//   one barrier, then
+//   warps 0..7, column group q of 4 columns each (lane = row r):
+//     3. X = A_(10) T'_(00) on the group's columns (A_(10) through its
+//        transposed copy A10T[i][r] = A[32 + r][i]), then
+//        T'_(10) = -T'_(11) X on the same columns, to T;
+//   warps 8..15 meanwhile copy T'_(00) and T'_(11) to T.
 __device__ void ut_transform(float* __restrict__ sA, float* __restrict__ Xs,
                              const float* __restrict__ A10T, const float* __restrict__ sBeta,
                              unsigned char* __restrict__ R, int tid) {
-  if (tid < 64) {
-    const int b = tid >> 4, j = tid & 15;
-    const float* Ab = sA + (16 * b) * kLdA + 16 * b;
-    float x[16];
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 2) {
+    const int h = warp;
+    {
+      const int b = 2 * h + (lane >> 4), j = lane & 15;
+      float* Ab = sA + (16 * b) * kLdA + 16 * b;
+      // row by row: x[r] = delta_rj - sum_{i < r} A[r][i] x[i], the terms in
+      // the order of i (the same sums as eliminating column by column)
+      float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+      for (int r = 0; r < 16; ++r) {
+        float acc = (r == j) ? 1.f : 0.f;
 #pragma unroll
-    for (int i = 0; i < 15; ++i) {
-      const float xi = x[i];
+        for (int i4 = 0; i4 < r; i4 += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(Ab + r * kLdA + i4);
 #pragma unroll
-      for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * kLdA + i], xi, x[r]);
+          for (int u = 0; u < 4; ++u)
+            if (i4 + u < r) acc = fmaf(-f4c(a4, u), x[i4 + u], acc);
+        }
+        x[r] = acc;
+      }
+      __syncwarp();  // both blocks of this warp are read
+#pragma unroll
+      for (int r = 0; r < 16; ++r) Ab[r * kLdA + j] = x[r];
     }
-    __syncwarp();  // every lane of this warp has read its block of A
-    float* Tb = sA + (16 * b) * kLdA + 16 * b;
+    __syncwarp();
+    {
+      const int a = 2 * h + 1, b = 2 * h;
+      const int r = lane >> 1, c0 = 8 * (lane & 1);
+      float* X = Xs + h * 256;  // [16][16]
+      float acc[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tb[r * kLdA + j] = x[r];
-  }
-  worker_sync();
-  {
-    // 16 -> 32: thread = (half h, row r, column c) of a 16 x 16 block
-    const int h = tid >> 8, r = (tid >> 4) & 15, c = tid & 15;
-    const int a = 2 * h + 1, b = 2 * h;
-    const float* Arow = sA + (16 * a + r) * kLdA + 16 * b;
-    const float* Dcol = sA + (16 * b) * kLdA + 16 * b + c;
-    float x = 0.f;
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      const float* Arow = sA + (16 * a + r) * kLdA + 16 * b;
+      const float* Db = sA + (16 * b) * kLdA + 16 * b + c0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x = fmaf(Arow[i], Dcol[i * kLdA], x);  // A_ab D_b
-    Xs[h * 256 + r * 16 + c] = x;
-    worker_sync();
-    const float* Drow = sA + (16 * a + r) * kLdA + 16 * a;
-    float y = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y = fmaf(Drow[i], Xs[h * 256 + i * 16 + c], y);  // D_a X
-    sA[(16 * a + r) * kLdA + 16 * b + c] = -y;
-  }
-  worker_sync();
-  {
-    // 32 -> 64, exploiting the triangular factors (warp-uniform loop bounds):
-    //   X = A_(10) T'_(00):  X[r][c] = sum_{i >= c} A10[r][i] T'00[i][c]
-    //     warps 0..7: 4 columns c = 4q .. 4q+3 each, lane = row r; A10 is read
-    //     through its transposed copy A10T[i][r] (conflict-free rows).  Column
-    //     group q costs 32 - 4q terms; q = w for w < 4, 11 - w above, so each
-    //     SM sub-partition (warps w and w + 4) gets the same work.
-    //   warps 8..15 meanwhile write T for the finished halves: rows 4w' .. 4w'+3
-    //     (w' = w - 8), lane = column.
-    if (tid < 256) {
-      const int w = tid >> 5, r = tid & 31;
-      const int q = w < 4 ? w : 11 - w;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i0 = 4 * q; i0 < 32; i0 += 4) {  // 4 steps per pass: the loads issue together
-        float av[4];
-        float4 t[4];
+      for (int i4 = 0; i4 < 16; i4 += 4) {
+        const float4 av = *reinterpret_cast<const float4*>(Arow + i4);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          av[u] = A10T[(i0 + u) * 32 + r];
-          t[u] = *reinterpret_cast<const float4*>(sA + (i0 + u) * kLdA + 4 * q);
+          const float4 d0 = *reinterpret_cast<const float4*>(Db + (i4 + u) * kLdA);
+          const float4 d1 = *reinterpret_cast<const float4*>(Db + (i4 + u) * kLdA + 4);
+          const float s = f4c(av, u);
+          acc[0] = fmaf(s, d0.x, acc[0]); acc[1] = fmaf(s, d0.y, acc[1]);
+          acc[2] = fmaf(s, d0.z, acc[2]); acc[3] = fmaf(s, d0.w, acc[3]);
+          acc[4] = fmaf(s, d1.x, acc[4]); acc[5] = fmaf(s, d1.y, acc[5]);
+          acc[6] = fmaf(s, d1.z, acc[6]); acc[7] = fmaf(s, d1.w, acc[7]);
         }
+      }
+      *reinterpret_cast<float4*>(X + r * 16 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(X + r * 16 + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      __syncwarp();
+      const float* Da = sA + (16 * a + r) * kLdA + 16 * a;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int i4 = 0; i4 < 16; i4 += 4) {
+        const float4 dv = *reinterpret_cast<const float4*>(Da + i4);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          x[0] = fmaf(av[u], t[u].x, x[0]);
-          x[1] = fmaf(av[u], t[u].y, x[1]);
-          x[2] = fmaf(av[u], t[u].z, x[2]);
-          x[3] = fmaf(av[u], t[u].w, x[3]);
+          const float4 x0 = *reinterpret_cast<const float4*>(X + (i4 + u) * 16 + c0);
+          const float4 x1 = *reinterpret_cast<const float4*>(X + (i4 + u) * 16 + c0 + 4);
+          const float s = f4c(dv, u);
+          acc[0] = fmaf(s, x0.x, acc[0]); acc[1] = fmaf(s, x0.y, acc[1]);
+          acc[2] = fmaf(s, x0.z, acc[2]); acc[3] = fmaf(s, x0.w, acc[3]);
+          acc[4] = fmaf(s, x1.x, acc[4]); acc[5] = fmaf(s, x1.y, acc[5]);
+          acc[6] = fmaf(s, x1.z, acc[6]); acc[7] = fmaf(s, x1.w, acc[7]);
         }
       }
-      *reinterpret_cast<float4*>(Xs + r * 36 + 4 * q) = make_float4(x[0], x[1], x[2], x[3]);
-    } else {
-      const int w8 = (tid >> 5) - 8, c = tid & 31;
-      const float b0 = sBeta[c], b1 = sBeta[32 + c];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = 4 * w8 + i;
-        put_T(R, r, c, sA[r * kLdA + c] * b0);                             // T'_(00)
-        put_T(R, 32 + r, 32 + c, sA[(32 + r) * kLdA + 32 + c] * b1);       // T'_(11)
-        // T'_(01) = 0
-        *reinterpret_cast<uint32_t*>(R + kRT + sw128_offset(C, r, 4 * (32 + c))) = 0u;
-        *reinterpret_cast<uint16_t*>(R + kRTh + sw128_offset(C, r, 2 * (32 + c))) = 0u;
-        *reinterpret_cast<uint16_t*>(R + kRTl + sw128_offset(C, r, 2 * (32 + c))) = 0u;
+      float* Tab = sA + (16 * a + r) * kLdA + 16 * b + c0;  // A_ab was read before the last sync
+      *reinterpret_cast<float4*>(Tab) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+      *reinterpret_cast<float4*>(Tab + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+    }
+  } else {
+    // T'_(01) = 0: rows 0..31, columns 32..63 of the tf32 copy (256 chunks of
+    // 16 bytes) and of the two bf16 copies (128 chunks each)
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid - 64; e < 512; e += 448) {
+      if (e < 256) {
+        *reinterpret_cast<uint4*>(R + kRT + sw128_offset(C, e >> 3, 16 * (8 + (e & 7)))) = z;
+      } else {
+        const int e2 = e - 256;
+        *reinterpret_cast<uint4*>(R + ((e2 >> 7) ? kRTl : kRTh) +
+                                  sw128_offset(C, (e2 & 127) >> 2, 64 + 16 * (e2 & 3))) = z;
       }
     }
-    worker_sync();
-    //   T'_(10) = -T'_(11) X:  rows 2p, 2p+1 per warp, lane = column c;
-    //     T'11[r][i] = 0 for i > r, so the loop stops at the warp's last row
-    //     (read 4 entries at a time: the zeros past the diagonal are harmless).
-    //     Row pair p costs 2p + 2 terms; p = k, 7 - k, 8 + k, 15 - k for the
-    //     four warps k, k + 4, k + 8, k + 12 of sub-partition k (equal sums).
-    const int w = tid >> 5, c = tid & 31;
-    const int k4 = w & 3, j4 = w >> 2;
-    const int p = j4 == 0 ? k4 : j4 == 1 ? 7 - k4 : j4 == 2 ? 8 + k4 : 15 - k4;
-    const float* T0 = sA + (32 + 2 * p) * kLdA + 32;
-    float y0 = 0.f, y1 = 0.f;
-    for (int i0 = 0; i0 <= 2 * p + 1; i0 += 4) {
-      const float4 a0 = *reinterpret_cast<const float4*>(T0 + i0);
-      const float4 a1 = *reinterpret_cast<const float4*>(T0 + kLdA + i0);
-      const float xv0 = Xs[i0 * 36 + c], xv1 = Xs[(i0 + 1) * 36 + c];
-      const float xv2 = Xs[(i0 + 2) * 36 + c], xv3 = Xs[(i0 + 3) * 36 + c];
-      y0 = fmaf(a0.x, xv0, y0); y0 = fmaf(a0.y, xv1, y0); y0 = fmaf(a0.z, xv2, y0); y0 = fmaf(a0.w, xv3, y0);
-      y1 = fmaf(a1.x, xv0, y1); y1 = fmaf(a1.y, xv1, y1); y1 = fmaf(a1.z, xv2, y1); y1 = fmaf(a1.w, xv3, y1);
+  }
+  worker_sync();
+  if (warp < 8) {
+    // column group q: q = w for w < 4, 11 - w above, so each SM sub-partition
+    // (warps w, w + 4) gets the same number of steps
+    const int q = warp < 4 ? warp : 11 - warp;
+    const int r = lane;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i0 = 4 * q; i0 < 32; i0 += 4) {  // T'_(00)[i][4q..] = 0 for i < 4q
+      float av[4];
+      float4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        av[u] = A10T[(i0 + u) * 32 + r];
+        t[u] = *reinterpret_cast<const float4*>(sA + (i0 + u) * kLdA + 4 * q);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[0] = fmaf(av[u], t[u].x, x[0]);
+        x[1] = fmaf(av[u], t[u].y, x[1]);
+        x[2] = fmaf(av[u], t[u].z, x[2]);
+        x[3] = fmaf(av[u], t[u].w, x[3]);
+      }
     }
-    const float bc = sBeta[c];
-    put_T(R, 32 + 2 * p, c, -y0 * bc);
-    put_T(R, 33 + 2 * p, c, -y1 * bc);
+    *reinterpret_cast<float4*>(Xs + r * 36 + 4 * q) = make_float4(x[0], x[1], x[2], x[3]);
+    __syncwarp();
+    // T'_(11) is stored in full (zeros above its diagonal): 32 terms per row
+    const float* T11 = sA + (32 + r) * kLdA + 32;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int i0 = 0; i0 < 32; i0 += 4) {
+      const float4 tv = *reinterpret_cast<const float4*>(T11 + i0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 xv = *reinterpret_cast<const float4*>(Xs + (i0 + u) * 36 + 4 * q);
+        const float s = f4c(tv, u);
+        y[0] = fmaf(s, xv.x, y[0]);
+        y[1] = fmaf(s, xv.y, y[1]);
+        y[2] = fmaf(s, xv.z, y[2]);
+        y[3] = fmaf(s, xv.w, y[3]);
+      }
+    }
+    const float4 bq = *reinterpret_cast<const float4*>(sBeta + 4 * q);
+    put_T4(R, 32 + r, q, make_float4(-y[0] * bq.x, -y[1] * bq.y, -y[2] * bq.z, -y[3] * bq.w));
+  } else {
+    // T'_(00) and T'_(11) to T: 2 halves x 32 rows x 8 column groups
+    for (int e = tid - 256; e < 512; e += 256) {
+      const int half = e >> 8, row = 32 * half + ((e >> 3) & 31), col = 32 * half + 4 * (e & 7);
+      const float4 tv = *reinterpret_cast<const float4*>(sA + row * kLdA + col);
+      const float4 bv = *reinterpret_cast<const float4*>(sBeta + col);
+      put_T4(R, row, col >> 2, make_float4(tv.x * bv.x, tv.y * bv.y, tv.z * bv.z, tv.w * bv.w));
+    }
   }
 }
 

@@ -199,9 +199,8 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t rows, uint32_
 
 // round-to-nearest fp32 -> tf32 (low 13 mantissa bits cleared)
 __device__ __forceinline__ uint32_t f32_to_tf32_rn(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+  // ties away from zero on the magnitude: add half an ulp of tf32, clear the low 13 bits
+  return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
