@@ -654,14 +654,14 @@ def main():
         tms, tk = time_decode_tokens(kb, decK, 20, args.warmup)
         n_sh = 256 * 32
         tbytes = n_sh * (8 * 128 * 128 + K * (12 * 128 + 4))
-        tn, tt = tk["kda_decode_step"]
+        tn, tt = tk["kda_decode_tokens"]
         t_gbs = tbytes / (tt / tn * 1e-3) / 1e9
         line["decode_tokens"] = {
             "workload": f"batched decode 256 seqs H32 d128, {K} tokens per call, all committed",
             "value": 256 * K / (tms * 1e-3), "unit": "tokens/s", "ms_per_call": tms,
             "roofline": {"bound": "hbm", "achieved": t_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": t_gbs / peaks["hbm_gbs"], "traffic": None,
-                         "kernel": "kda_decode_step", "peak_source": peak_src,
+                         "kernel": "kda_decode_tokens", "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": tbytes}}
         del decK
 

@@ -178,15 +178,8 @@ void launch_decode_t(const DecodeArgs& a, int64_t units, cudaStream_t s) {
 
 }  // namespace
 
-template <int D, bool FUSED>
-void launch_decode_t(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                     const float* log_alpha, const uint16_t* gate, const float* beta, float* S,
-                     uint16_t* out, int64_t units, cudaStream_t s) {
-  decode_kernel<D, FUSED><<<static_cast<unsigned>(units), DecodeCfg<D>::kThreads, 0, s>>>(
-      q, k, v, log_alpha, gate, beta, S, out);
-}
-
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  if (a.K > 1) return launch_decode_tokens(a, s);  // several tokens: the column-owner kernel
   const int64_t units = static_cast<int64_t>(a.N) * a.H;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   prof_begin(s, "kda_decode_step");

@@ -106,6 +106,8 @@ struct DecodeArgs {
   int* err;                 // device error word
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// K > 1 tokens per sequence (kda_decode_tokens.cu); launch_decode dispatches to it
+cudaError_t launch_decode_tokens(const DecodeArgs& a, cudaStream_t s);
 
 // bf16 helpers usable from device code without cuda_bf16.h conversions.
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {

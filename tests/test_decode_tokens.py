@@ -1,6 +1,6 @@
 """kda_decode_tokens: K tokens per sequence per call with a commit count
-(speculative decoding's verify / commit), against the fp64 oracle and
-against K single decode steps."""
+(speculative decoding's verify / commit), against the fp64 oracle, against
+K single decode steps, and across calls of different K."""
 import numpy as np
 import pytest
 import torch
@@ -53,26 +53,43 @@ def test_decode_tokens_commit_all_and_partial(d):
         np.testing.assert_array_equal(S.cpu().numpy()[zero], dec.S.numpy()[zero])
 
 
-def test_decode_tokens_equals_single_steps_bitwise():
-    """Verify (commit 0), then commit the accepted prefix: the result is exactly
-    the state after that many kda_decode_step calls."""
+def test_decode_tokens_verify_then_commit_is_exact():
+    """Verify (commit 0), then commit the accepted prefix: the verify call
+    writes no state, the outputs do not depend on the commit counts, and a
+    sequence that accepts c tokens ends bit-identical to a call over only its
+    first c tokens (the per-token arithmetic does not depend on K)."""
     dec = kin.make_decode(32, 4, 128, steps=6, seed=42)
     q, k, v, la, b = (t.cuda() for t in _seq_major(dec))
-    accept = np.array([6, 0, 3, 1] * 8, dtype=np.int32)
+    accept = np.array([6, 0, 3, 2] * 8, dtype=np.int32)
     S = dec.S.cuda()
     out_v = kb.kda_decode_tokens(q, k, v, la, b, S, torch.zeros(32, dtype=torch.int32, device="cuda"))
     assert torch.equal(S, dec.S.cuda())                       # verify wrote no state
     out_c = kb.kda_decode_tokens(q, k, v, la, b, S, torch.from_numpy(accept).cuda())
     assert torch.equal(out_v, out_c)                          # outputs do not depend on commit
-    S1 = dec.S.cuda()                 # state of the sequential single steps
-    S_ref = dec.S.cuda().clone()      # expected committed state (accept 0: the start)
-    for t in range(6):
-        o = kb.kda_decode_step(q[:, t].contiguous(), k[:, t].contiguous(), v[:, t].contiguous(),
-                               la[:, t].contiguous(), b[:, t].contiguous(), S1)
-        assert torch.equal(o, out_c[:, t])
-        done = torch.from_numpy(accept == t + 1).cuda()
-        S_ref[done] = S1[done]
-    assert torch.equal(S, S_ref)
+    for c in (6, 3, 2):
+        Sc = dec.S.cuda()
+        o = kb.kda_decode_tokens(q[:, :c].contiguous(), k[:, :c].contiguous(),
+                                 v[:, :c].contiguous(), la[:, :c].contiguous(),
+                                 b[:, :c].contiguous(), Sc)
+        assert torch.equal(o, out_c[:, :c])
+        sel = torch.from_numpy(accept == c).cuda()
+        assert torch.equal(S[sel], Sc[sel])
+    assert torch.equal(S[torch.from_numpy(accept == 0).cuda()],
+                       dec.S.cuda()[torch.from_numpy(accept == 0).cuda()])
+
+
+def test_decode_tokens_matches_single_steps():
+    """K tokens in one call against K calls of the single step (a separate
+    kernel): same outputs and state up to rounding."""
+    dec = kin.make_decode(64, 8, 128, steps=5, seed=44)
+    q, k, v, la, b = (t.cuda() for t in _seq_major(dec))
+    S = dec.S.cuda()
+    out = kb.kda_decode_tokens(q, k, v, la, b, S)
+    S1 = dec.S.cuda()
+    outs = [kb.kda_decode_step(q[:, t].contiguous(), k[:, t].contiguous(), v[:, t].contiguous(),
+                               la[:, t].contiguous(), b[:, t].contiguous(), S1) for t in range(5)]
+    check_out(out.float().cpu().numpy(), torch.stack(outs, 1).float().cpu().numpy())
+    check_state(S.cpu().numpy(), S1.cpu().numpy())
 
 
 def test_decode_tokens_rejects_commit_out_of_range():
