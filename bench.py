@@ -660,7 +660,8 @@ def main():
             "workload": f"batched decode 256 seqs H32 d128, {K} tokens per call, all committed",
             "value": 256 * K / (tms * 1e-3), "unit": "tokens/s", "ms_per_call": tms,
             "roofline": {"bound": "hbm", "achieved": t_gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": t_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": t_gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("kda_decode_tokens", "kda_decode_tokens.cu"),
                          "kernel": "kda_decode_tokens", "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": tbytes}}
         del decK
