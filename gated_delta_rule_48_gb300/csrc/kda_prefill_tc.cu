@@ -415,11 +415,20 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   const Segment sg = a.plan.segs[seg_id];
   const bool last = sg.index + 1 == sg.count;
   if (MODE == kModeSummary && last) return;
-  // summary units: z = 0 accumulates the increment B (values, zero start),
-  // z = 1 the transition M (no values, identity start)
-  const bool ident = MODE == kModeSummary && blockIdx.z == 1;
-  const bool has_v = !ident;
+  // A summary unit carries two states through the segment: the increment B
+  // (its values, from zero) and the transition M (no values, from the
+  // identity).  They share the decay scan, the strip products, T, W and K';
+  // only the state-reading products and the state updates are doubled.
   constexpr bool kOut = MODE == kModeReplay;
+  constexpr bool kSum = MODE == kModeSummary;
+  // TMEM columns of this mode.  Replay: S^T 0, strip products 128, W^T 256,
+  // U^T 320, O^T 384.  Summary: S_B^T 0, S_M^T 128, U_B^T 256, U_M^T 320, and
+  // the strip products share 384.. with W^T: W^T of chunk n is read out (phase
+  // D) before the strip MMA of chunk n+1 is issued, by the issuer that wrote it.
+  constexpr uint32_t cA = kSum ? 384 : kColA;
+  constexpr uint32_t cW = kSum ? 384 : kColW;
+  constexpr uint32_t cU = kSum ? 256 : kColU;
+  constexpr uint32_t cSM = 128, cUM = 320;  // summary only
   const int H = a.H;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -530,12 +539,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         const int c = 32 * part + cc + x;
-        float v = 0.f;
-        if (ident) v = (c == j) ? 1.f : 0.f;
-        else if (src) v = src[c * D + j];
-        r[x] = __float_as_uint(v);
+        r[x] = __float_as_uint(src ? src[c * D + j] : 0.f);
       }
       tmem_st16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), r);
+      if (kSum) {  // S_M = I
+#pragma unroll
+        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(32 * part + cc + x == j ? 1.f : 0.f);
+        tmem_st16(tmem_addr(tmem, 32 * quad, cSM + 32 * part + cc), r);
+      }
     }
     tmem_wait_st();
   }
@@ -704,16 +715,39 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
 
   // S^T (TMEM) -> dst[c * ld + j] = S[c][j] (row = key channel), f32; worker warps.
-  auto store_state = [&](float* dst, int64_t ld) {
+  auto store_state = [&](float* dst, int64_t ld, uint32_t col) {
     const int j = 32 * quad + lane;
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
       uint32_t sv[16];
-      tmem_ld16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
+      tmem_ld16(tmem_addr(tmem, 32 * quad, col + 32 * part + cc), sv);
       tmem_wait_ld();
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
     }
+  };
+  // Phase F on one state: decay the columns of S^T (TMEM columns cs..) by
+  // e^{g_last} of chunk n, round U^T (columns cu..) to tf32 in place.
+  auto decay_round = [&](uint32_t cs, uint32_t cu, int64_t n) {
+#pragma unroll
+    for (int cc = 0; cc < 32; cc += 16) {
+      const uint32_t ta = tmem_addr(tmem, 32 * quad, cs + 32 * part + cc);
+      uint32_t sv[16];
+      tmem_ld16(ta, sv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[(n & 1) * 128 + 32 * part + cc + x]);
+      tmem_st16(ta, sv);
+    }
+    const uint32_t tu = tmem_addr(tmem, 32 * quad, cu + 16 * part);
+    uint32_t uv[16];
+    tmem_ld16(tu, uv);
+    tmem_wait_ld();
+#pragma unroll
+    for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
+    tmem_st16(tu, uv);
+    tmem_wait_st();
   };
   // ================= control warps: issue the MMA groups once their operands are ready.
   // Issuing a tcgen05.mma costs the issuing thread ~100 cycles, far more than
@@ -731,7 +765,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     auto kdesc = [](const void* p) { return smem_desc_sw128(smem_u32(p), 16, 1024); };
     if (who == 1 && n_chunks > 0) {
       issue_qkl(sg.t0);
-      if (has_v) issue_v(sg.t0);
+      issue_v(sg.t0);
     }
     for (int64_t n = 0; n < n_chunks; ++n) {
       if (who == 1) {  // raw q, k, log_alpha of chunk n read by every worker: stream in n+1
@@ -752,7 +786,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
               const uint64_t a0 = kdesc(R), b0 = kdesc(R + 32768);
 #pragma unroll 4
               for (int j = 0; j < D / 16; ++j)
-                mma_f16_ss(tmem + kColA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
+                mma_f16_ss(tmem + cA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
             }
             mma_commit(bar_done + 0);
           }
@@ -763,38 +797,43 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
               const uint64_t kg = kdesc(KG), tt = kdesc(R + kRT);
 #pragma unroll 4
               for (int j = 0; j < C / 8; ++j)
-                mma_tf32_ss(tmem + kColW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
+                mma_tf32_ss(tmem + cW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
             }
           } else {  // U~^T = V^T T^T (bf16 hi + lo), once raw v has landed
             bool ok = go;
-            if (ok && has_v && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+            if (ok && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
             tc_fence_after();
-            if (ok && has_v) {
+            if (ok) {
               const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
               const uint64_t vv = smem_desc_sw128(smem_u32(sm + kRawV), 64 * 128, 1024);
               const uint64_t th = kdesc(R + kRTh), tl = kdesc(R + kRTl);
 #pragma unroll 4
               for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
                 const int jj = j & 3;
-                mma_f16_ss(tmem + kColU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
+                mma_f16_ss(tmem + cU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
                            idu, j > 0);
               }
             }
           }
           mma_commit(bar_done + 1);
           // raw v of chunk n consumed once group 1 has completed: stream in n+1
-          if (who == 1 && has_v && n + 1 < n_chunks) {
+          if (who == 1 && n + 1 < n_chunks) {
             if (mbar_wait(bar_done + 1, static_cast<uint32_t>(n & 1))) issue_v(sg.t0 + (n + 1) * C);
             else flag_timeout();
           }
         } else if (g == 2) {
           const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-          if (go && who == 0) {  // U^T -= S^T W^T
+          if (go && who == 0) {  // U^T -= S^T W^T (KG holds -W)
             const uint64_t wm = kdesc(KG);
 #pragma unroll 4
             for (int j = 0; j < D / 8; ++j)
-              mma_tf32_ts(tmem + kColU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id,
-                          (has_v || j > 0) ? 1u : 0u);
+              mma_tf32_ts(tmem + cU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id, 1);
+          }
+          if (go && who == 1 && kSum) {  // U_M^T = -S_M^T W^T (no values)
+            const uint64_t wm = kdesc(KG);
+#pragma unroll 4
+            for (int j = 0; j < D / 8; ++j)
+              mma_tf32_ts(tmem + cUM, tmem + cSM + 8 * j, kmaj(wm, j, 64 * 128), id, j > 0);
           }
           if (go && who == 1 && kOut) {  // O^T = S^T (q e^g)^T
             const uint64_t qg = kdesc(R + kRQ);
@@ -809,14 +848,21 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             const uint64_t aq = kdesc(R + kRAqk);
 #pragma unroll 4
             for (int j = 0; j < C / 8; ++j)
-              mma_tf32_ts(tmem + kColO, tmem + kColU + 8 * j, kmaj(aq, j, 64 * 128), id, 1);
+              mma_tf32_ts(tmem + kColO, tmem + cU + 8 * j, kmaj(aq, j, 64 * 128), id, 1);
+          }
+          if (go && who == 1 && kSum) {  // S_M^T += U_M^T K'
+            const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+            const uint64_t kp = kdesc(KP);
+#pragma unroll 4
+            for (int j = 0; j < C / 8; ++j)
+              mma_tf32_ts(tmem + cSM, tmem + cUM + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
           }
           if (go && who == 0) {  // S^T += U^T K'
             const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
             const uint64_t kp = kdesc(KP);
 #pragma unroll 4
             for (int j = 0; j < C / 8; ++j)
-              mma_tf32_ts(tmem + kColS, tmem + kColU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
+              mma_tf32_ts(tmem + kColS, tmem + cU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
           }
           mma_commit(bar_done + 3);
         }
@@ -855,7 +901,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         const int nk = s ? 16 : 8;  // keys handled by this warp: [i0, i0 + nk)
         const int i0 = part * nk;
         uint32_t v[16];
-        const uint32_t ta = tmem_addr(tmem, 32 * quad, kColA + (s ? 32u : 0u) + i0);
+        const uint32_t ta = tmem_addr(tmem, 32 * quad, cA + (s ? 32u : 0u) + i0);
         if (s) tmem_ld16(ta, v); else tmem_ld8(ta, v);
         tmem_wait_ld();
         const float b = sBeta[r];
@@ -927,7 +973,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       {
         const int c = 32 * quad + lane;
         uint32_t w[16];
-        tmem_ld16(tmem_addr(tmem, 32 * quad, kColW + 16 * part), w);
+        tmem_ld16(tmem_addr(tmem, 32 * quad, cW + 16 * part), w);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 16; ++x)
@@ -955,27 +1001,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (*s_abort) break;
 
       // ---- F: decay the columns of S^T by e^{g_last}; round U^T to tf32
-      {
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
-          const uint32_t ta = tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc);
-          uint32_t sv[16];
-          tmem_ld16(ta, sv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[(n & 1) * 128 + 32 * part + cc + x]);
-          tmem_st16(ta, sv);
-        }
-        const uint32_t tu = tmem_addr(tmem, 32 * quad, kColU + 16 * part);
-        uint32_t uv[16];
-        tmem_ld16(tu, uv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 16; ++x) uv[x] = f32_to_tf32_rn(__uint_as_float(uv[x]));
-        tmem_st16(tu, uv);
-        tmem_wait_st();
-      }
+      //      (summary: both S_B^T and S_M^T, U_B^T and U_M^T)
+      decay_round(kColS, cU, n);
+      if (kSum) decay_round(cSM, cUM, n);
       signal_ready(3);  // S^T decayed, U^T rounded, A_qk and K' in SMEM
 
       // ---- G: O^T += U^T A_qk^T ; S^T += U^T K'  (A = U^T)  ||  chunk n+1 operand build
@@ -1012,15 +1040,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 
     // ---- the segment's final state (S^T in TMEM) to global memory
     if (!*s_abort) {
-      float* dst = nullptr;
-      int64_t ld = D;  // row stride of the destination (floats)
       if (MODE == kModeReplay) {
-        if (last && a.S_final) dst = a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * D * D;
-      } else {
-        ld = 2 * D;  // increment | transition record
-        dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D) + (ident ? D : 0);
+        if (last && a.S_final)
+          store_state(a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * D * D, D, kColS);
+      } else {  // the increment | transition record, rows of 2 D floats
+        float* dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D);
+        store_state(dst, 2 * D, kColS);
+        store_state(dst + D, 2 * D, cSM);
       }
-      if (dst) store_state(dst, ld);
     }
   }  // worker warps
   tc_fence_before();
@@ -1096,7 +1123,7 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.plan.capacity, a.H, MODE == kModeSummary ? 2 : 1);
+  dim3 grid(a.plan.capacity, a.H, 1);
   prof_begin(s, name);
   prefill_tc_kernel<MODE, FUSED, CKPT><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
