@@ -107,7 +107,7 @@ constexpr uint32_t kEGl = kGl + 512;          // e^{g_last} [2][128], by chunk p
 constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e^{G0}, e^{G1},
                                               // e^{g_last - G0}, e^{g_last - G1}, e^{G1 - G0}
 constexpr uint32_t kBeta = kPC + 5 * 512;
-constexpr uint32_t kBars = kBeta + 256;       // 11 mbarriers, TMEM slot, abort flag
+constexpr uint32_t kBars = kBeta + 256;       // 12 mbarriers, TMEM slot, abort flag
 constexpr uint32_t kSmemBytes = kBars + 128 + 1024;  // + alignment slack
 static_assert(kRXs + 32 * 36 * 4 <= kRAqk, "UT scratch overlaps A_qk");
 static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
@@ -231,9 +231,11 @@ __device__ __forceinline__ float f4c(const float4& v, int u) {  // component u (
 //        transposed copy A10T[i][r] = A[32 + r][i]), then
 //        T'_(10) = -T'_(11) X on the same columns, to T;
 //   warps 8..15 meanwhile copy T'_(00) and T'_(11) to T.
-__device__ void ut_transform(float* __restrict__ sA, float* __restrict__ Xs,
-                             const float* __restrict__ A10T, const float* __restrict__ sBeta,
-                             unsigned char* __restrict__ R, int tid) {
+// Split at its one barrier: ut_front (steps 1, 2 and the zeros), then the
+// caller's worker barrier, then ut_back (step 3 and the copies).  Warps 2..15
+// are free between ut_front and the barrier.
+__device__ void ut_front(float* __restrict__ sA, float* __restrict__ Xs,
+                         unsigned char* __restrict__ R, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 2) {
     const int h = warp;
@@ -321,7 +323,12 @@ __device__ void ut_transform(float* __restrict__ sA, float* __restrict__ Xs,
       }
     }
   }
-  worker_sync();
+}
+
+__device__ void ut_back(float* __restrict__ sA, float* __restrict__ Xs,
+                        const float* __restrict__ A10T, const float* __restrict__ sBeta,
+                        unsigned char* __restrict__ R, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
   if (warp < 8) {
     // column group q: q = w for w < 4, 11 - w above, so each SM sub-partition
     // (warps w, w + 4) gets the same number of steps
@@ -429,6 +436,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   constexpr uint32_t cW = kSum ? 384 : kColW;
   constexpr uint32_t cU = kSum ? 256 : kColU;
   constexpr uint32_t cSM = 128, cUM = 320;  // summary only
+  // Replay computes U^T = U~^T - P^T T^T with P^T = S^T (k e^g)^T (TMEM, in W^T's
+  // columns): P^T needs only the state at the chunk's start and k e^g, so it
+  // is issued with the strip products, and no W^T goes through SMEM.
+  // Summary keeps U^T = U~^T - S^T W^T (two states' P^T would not fit TMEM).
+  constexpr bool kP = kOut;
+  constexpr uint32_t cP = kColW;
   const int H = a.H;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -437,7 +450,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   uint64_t* bar_done = bars + 2;   // [4] MMA group committed: 0 strip, 1 WY, 2 S-read, 3 state
   uint64_t* bar_ready = bars + 6;  // [4] operands of that group ready (one arrive per worker warp)
   uint64_t* bar_raw = bars + 10;   // raw q, k, log_alpha of a chunk read (one arrive per worker warp)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* bar_donep = bars + 11; // replay: P^T = S^T (k e^g)^T committed (issuer 1)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   float* sTot = reinterpret_cast<float*>(sm + kTot);
   float* sG0 = reinterpret_cast<float*>(sm + kG0);
@@ -465,6 +479,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       mbar_init(bar_ready + g, kWarps);
     }
     mbar_init(bar_raw, kWarps);
+    mbar_init(bar_donep, 1);
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -649,8 +664,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
 
   // Operand build of the scanned chunk: strip operands (bf16) and k e^g
-  // (transposed, tf32) into SMEM, made visible to the tensor core.  Reads cr
-  // and sPC (written by scan_chunk, separated from here by a barrier).
+  // (tf32) into SMEM, made visible to the tensor core: replay stores k e^g
+  // [token][channel] (the B operand of P^T = S^T (k e^g)^T), summary
+  // transposed (the A operand of W^T = (k e^g)^T T^T).  Reads cr and sPC
+  // (written by scan_chunk, separated from here by a barrier).
   auto build_chunk = [&]() {
     unsigned char* Aop = R;           // bf16 [128][128]: strip s -> rows 64 s + (q: 0 | k: 32) + rr
     unsigned char* Bop = R + 32768;   // bf16 [96][128]: keys 0..31 (strip-0 anchor) | keys 0..63
@@ -672,6 +689,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         kh[x] = kf[x] * inv;
         kgT[x][i] = kt[x] * eG[x];
       }
+      if (kP) *reinterpret_cast<uint4*>(KG + sw128_offset(C, r, 16 * lane)) =
+          make_uint4(f32_to_tf32_rn(kgT[0][i]), f32_to_tf32_rn(kgT[1][i]),
+                     f32_to_tf32_rn(kgT[2][i]), f32_to_tf32_rn(kgT[3][i]));
       *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + rr, 8 * lane)) = pack4_bf16(qt);
       *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + 32 + rr, 8 * lane)) =
           pack4_bf16(kt);
@@ -685,10 +705,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh);
       }
     }
-    uint4 kv[4];
+    if (!kP) {
+      uint4 kv[4];
 #pragma unroll
-    for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kgT[x]);
-    st_transposed4(KG, lane, r0, kv);
+      for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kgT[x]);
+      st_transposed4(KG, lane, r0, kv);
+    }
     fence_proxy_async_smem();
   };
 
@@ -728,6 +750,38 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
   // Phase F on one state: decay the columns of S^T (TMEM columns cs..) by
   // e^{g_last} of chunk n, round U^T (columns cu..) to tf32 in place.
+  // Replay, warps 2..15: -P^T rounded to tf32 in place.  A warp reaches the
+  // TMEM lanes of its quadrant (warp mod 4); the 4 blocks of 16 columns go
+  // round-robin over that quadrant's warps (4, 8, 12 + q for q = 0, 1; q, 4,
+  // 8, 12 + q for q = 2, 3).
+  auto round_neg_p = [&]() {
+    const int first = quad < 2 ? 4 + quad : quad, cnt = quad < 2 ? 3 : 4;
+#pragma unroll 1
+    for (int c = (warp - first) >> 2; c < 4; c += cnt) {
+      const uint32_t ta = tmem_addr(tmem, 32 * quad, cP + 16 * c);
+      uint32_t pv[16];
+      tmem_ld16(ta, pv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int x = 0; x < 16; ++x) pv[x] = f32_to_tf32_rn(-__uint_as_float(pv[x]));
+      tmem_st16(ta, pv);
+      tmem_wait_st();
+    }
+  };
+  // Replay: q e^g = q e^{g - G} e^G of this warp's tokens, [token][channel]
+  // tf32 into KG (the B operand of O^T = S^T (q e^g)^T)
+  auto write_qeg = [&]() {
+    const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
+    const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float qf[4], f[4];
+      unpack4(cr.qraw[i], qf);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * eG[x];
+      *reinterpret_cast<uint4*>(KG + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
+    }
+  };
   auto decay_round = [&](uint32_t cs, uint32_t cu, int64_t n) {
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
@@ -773,6 +827,97 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         if (!mbar_wait(bar_raw, static_cast<uint32_t>(n & 1))) { flag_timeout(); break; }
         if (n + 1 < n_chunks) issue_qkl(sg.t0 + (n + 1) * C);
       }
+      if constexpr (kP) {  // replay: groups 0 | P, 1, 3
+        const uint32_t id64 = make_idesc(kFmtTF32, 128, 64, false, false);
+        // group 0: strip products (issuer 0); P^T = S^T (k e^g)^T once the
+        // previous chunk's state update has completed (issuer 1)
+        bool ready = mbar_wait(bar_ready + 0, static_cast<uint32_t>(n & 1));
+        if (ready && who == 1 && n > 0)
+          ready = mbar_wait(bar_done + 3, static_cast<uint32_t>((n - 1) & 1));
+        if (!ready) flag_timeout();
+        tc_fence_after();
+        bool go = ready && !*s_abort;
+        if (who == 0) {
+          if (go) {
+            const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
+            const uint64_t a0 = kdesc(R), b0 = kdesc(R + 32768);
+#pragma unroll 2
+            for (int j = 0; j < D / 16; ++j)
+              mma_f16_ss(tmem + cA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
+          }
+          mma_commit(bar_done + 0);
+        } else {
+          if (go) {
+            const uint64_t kg = kdesc(KG);
+#pragma unroll 2
+            for (int j = 0; j < D / 8; ++j)
+              mma_tf32_ts(tmem + cP, tmem + kColS + 8 * j, kmaj(kg, j, 64 * 128), id64, j > 0);
+          }
+          mma_commit(bar_donep);
+        }
+        if (*s_abort) break;
+        // group 1: O^T = S^T (q e^g)^T (issuer 0); U^T = V^T T^T (bf16 hi + lo)
+        // + (-P^T) T^T (issuer 1)
+        ready = mbar_wait(bar_ready + 1, static_cast<uint32_t>(n & 1));
+        if (!ready) flag_timeout();
+        tc_fence_after();
+        go = ready && !*s_abort;
+        if (who == 0) {
+          if (go) {
+            const uint64_t qg = kdesc(KG);
+#pragma unroll 2
+            for (int j = 0; j < D / 8; ++j)
+              mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, kmaj(qg, j, 64 * 128), id64, j > 0);
+          }
+          mma_commit(bar_done + 1);
+        } else {
+          bool ok = go;
+          if (ok && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+          tc_fence_after();
+          if (ok) {
+            const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
+            const uint64_t vv = smem_desc_sw128(smem_u32(sm + kRawV), 64 * 128, 1024);
+            const uint64_t th = kdesc(R + kRTh), tl = kdesc(R + kRTl);
+#pragma unroll 2
+            for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
+              const int jj = j & 3;
+              mma_f16_ss(tmem + cU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
+                         idu, j > 0);
+            }
+            const uint64_t tt = kdesc(R + kRT);
+#pragma unroll 2
+            for (int j = 0; j < C / 8; ++j)
+              mma_tf32_ts(tmem + cU, tmem + cP + 8 * j, kmaj(tt, j, 64 * 128), id64, 1);
+          }
+          mma_commit(bar_done + 1);
+          // raw v of chunk n consumed once group 1 has completed: stream in n+1
+          if (n + 1 < n_chunks) {
+            if (mbar_wait(bar_done + 1, static_cast<uint32_t>(n & 1))) issue_v(sg.t0 + (n + 1) * C);
+            else flag_timeout();
+          }
+        }
+        if (*s_abort) break;
+        // group 3: S^T += U^T K' (issuer 0); O^T += U^T A_qk^T (issuer 1)
+        ready = mbar_wait(bar_ready + 3, static_cast<uint32_t>(n & 1));
+        if (!ready) flag_timeout();
+        tc_fence_after();
+        go = ready && !*s_abort;
+        if (go && who == 0) {
+          const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+          const uint64_t kp = kdesc(KP);
+#pragma unroll 2
+          for (int j = 0; j < C / 8; ++j)
+            mma_tf32_ts(tmem + kColS, tmem + cU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
+        }
+        if (go && who == 1) {
+          const uint64_t aq = kdesc(R + kRAqk);
+#pragma unroll 2
+          for (int j = 0; j < C / 8; ++j)
+            mma_tf32_ts(tmem + kColO, tmem + cU + 8 * j, kmaj(aq, j, 64 * 128), id64, 1);
+        }
+        mma_commit(bar_done + 3);
+        if (*s_abort) break;
+      } else {  // summary: groups 0..3
       for (int g = 0; g < 4; ++g) {
         if (*s_abort) break;
         const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
@@ -867,6 +1012,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           mma_commit(bar_done + 3);
         }
       }
+      }
       if (*s_abort) break;
     }
   };
@@ -943,9 +1089,26 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       // query-row warps (A_qk) join at the inverse's next barrier, so their
       // longer read-out overlaps the diagonal blocks.
       if (warp == 0 || (warp & 1)) asm volatile("bar.sync 2, 288;" ::: "memory");
-      ut_transform(sAkk, reinterpret_cast<float*>(R + kRXs), reinterpret_cast<const float*>(KP),
-                   sBeta, R, tid);
-      signal_ready(1);  // T, k e^g, V ready for the WY products
+      ut_front(sAkk, reinterpret_cast<float*>(R + kRXs), R, tid);
+      // replay: once P^T has landed, -P^T rounded to tf32 in TMEM (warps 2..15,
+      // which are free here) and q e^g into KG (P^T's B operand is consumed);
+      // warps 0 and 1 write their q e^g after the transform
+      if (kP && warp >= 2) {
+        if (!mbar_wait(bar_donep, static_cast<uint32_t>(n & 1))) flag_timeout();
+        tc_fence_after();
+        round_neg_p();
+        write_qeg();
+      }
+      worker_sync();
+      ut_back(sAkk, reinterpret_cast<float*>(R + kRXs), reinterpret_cast<const float*>(KP), sBeta,
+              R, tid);
+      if (kP && warp < 2) {
+        if (!mbar_wait(bar_donep, static_cast<uint32_t>(n & 1))) flag_timeout();
+        tc_fence_after();
+        write_qeg();
+      }
+      if (kP) worker_sync();  // K' and the next scan start after the transform's critical step
+      signal_ready(1);  // T, V (and k e^g | -P^T, q e^g) ready for group 1
 
       // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
       {
@@ -965,11 +1128,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kp[x]);
         st_transposed4(KP, lane, r0, kv);
       }
+      if (kP && n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
       wait_done(1, n);
       worker_sync();
       if (*s_abort) break;
 
-      // ---- D: -W (from W^T in TMEM, lane = key channel) and q e^g to SMEM
+      if (!kP) {  // summary: phases D and E
+
+      // ---- D: -W (from W^T in TMEM, lane = key channel) to SMEM
       {
         const int c = 32 * quad + lane;
         uint32_t w[16];
@@ -979,26 +1145,15 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         for (int x = 0; x < 16; ++x)
           *reinterpret_cast<uint32_t*>(KG + sw128_offset(C, 16 * part + x, 4 * c)) =
               f32_to_tf32_rn(-__uint_as_float(w[x]));
-        if (kOut) {
-          const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
-          const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float qf[4], f[4];
-            unpack4(cr.qraw[i], qf);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * eG[x];
-            *reinterpret_cast<uint4*>(R + kRQ + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
-          }
-        }
       }
-      signal_ready(2);  // -W and q e^g ready
+      signal_ready(2);  // -W ready
 
-      // ---- E: U^T -= S^T W^T ; O^T = S^T (q e^g)^T (A = S^T in TMEM) || scan of chunk n+1
+      // ---- E: U^T -= S^T W^T (A = S^T in TMEM)  ||  scan of chunk n+1
       if (n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
       wait_done(2, n);
       worker_sync();
       if (*s_abort) break;
+      }
 
       // ---- F: decay the columns of S^T by e^{g_last}; round U^T to tf32
       //      (summary: both S_B^T and S_M^T, U_B^T and U_M^T)
