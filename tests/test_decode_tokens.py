@@ -53,6 +53,39 @@ def test_decode_tokens_commit_all_and_partial(d):
         np.testing.assert_array_equal(S.cpu().numpy()[zero], dec.S.numpy()[zero])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_tokens_several_batches(d):
+    """K = 19 tokens: three batches of the kernel's 8, with commits before,
+    at and after the batch boundaries (the state is carried across them)."""
+    K = 19
+    dec = kin.make_decode(24, 3, d, steps=K, seed=45)
+    q, k, v, la, b = _seq_major(dec)
+    commit = np.array([19, 0, 8, 9, 16, 17, 1, 12] * 3, dtype=np.int32)
+    S = dec.S.cuda()
+    out = kb.kda_decode_tokens(q.cuda(), k.cuda(), v.cuda(), la.cuda(), b.cuda(), S,
+                               torch.from_numpy(commit).cuda())
+    assert kb.kda_get_device_error() == 0
+    ref_o, ref_S = _oracle(q, k, v, la, b, dec.S, commit)
+    check_out(out.float().cpu().numpy(), ref_o)
+    check_state(S.cpu().numpy(), ref_S)
+
+
+def test_decode_tokens_two_tokens_strong_and_weak_decay():
+    """K = 2 (the smallest multi-token call) with log alpha at the clamp (-5)
+    on half the channels and 0 (no decay) on the rest."""
+    dec = kin.make_decode(40, 2, 128, steps=2, seed=46)
+    la = dec.log_alpha.clone()
+    la[..., :64] = -5.0
+    la[..., 64:] = 0.0
+    dec.log_alpha = la
+    q, k, v, la, b = _seq_major(dec)
+    S = dec.S.cuda()
+    out = kb.kda_decode_tokens(q.cuda(), k.cuda(), v.cuda(), la.cuda(), b.cuda(), S)
+    ref_o, ref_S = _oracle(q, k, v, la, b, dec.S, np.full(40, 2))
+    check_out(out.float().cpu().numpy(), ref_o)
+    check_state(S.cpu().numpy(), ref_S)
+
+
 def test_decode_tokens_verify_then_commit_is_exact():
     """Verify (commit 0), then commit the accepted prefix: the verify call
     writes no state, the outputs do not depend on the commit counts, and a

@@ -111,3 +111,26 @@ def test_fused_decode_tokens_with_commit():
                                   flat(b).numpy()[keep], r.S.numpy(),
                                   np.concatenate([[0], np.cumsum(commit)]))
     check_state(S.cpu().numpy(), ref_S)
+
+
+def test_fused_decode_tokens_several_batches():
+    """Raw projections, K = 11 (two batches of the kernel's 8), partial commits."""
+    K, N = 11, 16
+    r = kin.make_decode_raw(N, 2, 128, steps=K, seed=37)
+    f = lambda t: t.transpose(0, 1).contiguous()
+    q, k, v, g, b = (f(t) for t in (r.q_raw, r.k_raw, r.v, r.gate, r.beta))
+    commit = np.array([11, 0, 7, 8, 9, 3, 10, 1] * 2, dtype=np.int32)
+    S = r.S.cuda()
+    out = kb.kda_decode_tokens_fused(q.cuda(), k.cuda(), v.cuda(), g.cuda(), b.cuda(), S,
+                                     torch.from_numpy(commit).cuda())
+    assert kb.kda_get_device_error() == 0
+    flat = lambda t: t.reshape((N * K,) + tuple(t.shape[2:]))
+    bits = lambda t: kin.bf16_bits(flat(t))
+    ref_o, _ = prep.forward_fused(bits(q), bits(k), bits(v), bits(g), flat(b).numpy(), r.S.numpy(),
+                                  np.arange(N + 1) * K)
+    check_out(out.float().cpu().numpy().reshape(ref_o.shape), ref_o)
+    keep = np.concatenate([np.arange(n * K, n * K + c) for n, c in enumerate(commit)]).astype(int)
+    _, ref_S = prep.forward_fused(bits(q)[keep], bits(k)[keep], bits(v)[keep], bits(g)[keep],
+                                  flat(b).numpy()[keep], r.S.numpy(),
+                                  np.concatenate([[0], np.cumsum(commit)]))
+    check_state(S.cpu().numpy(), ref_S)
