@@ -30,8 +30,10 @@ struct DecodeCfg {
   static constexpr int kRowsPerThread = D / kRowGroups;     // 16 or 8
 };
 
-// K tokens per sequence, applied in order from the state in registers (K = 1
-// is the plain step).  Token t of sequence n is row n*K + t of the packed
+// K tokens per sequence, applied in order from the state in registers.
+// launch_decode runs it for K = 1, the plain step; calls with K > 1 go to the
+// persistent multi-token kernel (kda_decode_tokens.cu), which computes the
+// same recurrence faster at K > 1.  Token t of sequence n is row n*K + t of the packed
 // inputs: q, k, log_alpha [N*K, H, dk], v [N*K, H, dv], beta [N*K, H], out
 // [N*K, H, dv].  Every token's output is written; the state in memory
 // advances by the first `commit[n]` tokens only (commit == null: all K),

@@ -1,7 +1,7 @@
 // Chunk-parallel prefill on the tcgen05 tensor cores (dk = dv = 128).
 //
-// One CTA per unit = (segment, head[, column kind]) walks the segment's
-// 64-token chunks in order.  The state is kept TRANSPOSED in tensor memory
+// One CTA per unit = (segment, head) walks the segment's 64-token chunks in
+// order.  The state is kept TRANSPOSED in tensor memory
 // (S^T: lane = value channel j, column = key channel c, fp32) for the whole
 // segment and is itself the A operand of the MMAs that read it, so it never
 // leaves the SM between chunks.  Per chunk (tokens r, i of the chunk, g the
@@ -10,9 +10,10 @@
 //   strip products (bf16):  A_qk[r,i] = sum_c q_rc k_ic e^{g_rc - g_ic}  (i <= r)
 //                           A_kk[r,i] = beta_r sum_c k_rc k_ic e^{g_rc - g_ic}  (i < r)
 //   UT transform (fp32):    T = (I + A_kk)^{-1} Diag(beta)
-//   WY products:            W^T = (k e^g)^T T^T (tf32),  U~^T = V^T T^T (bf16 hi + lo)
-//   hand-off (tf32):        U^T = U~^T - S^T W^T
-//                           O^T = S^T (q e^g)^T + U^T A_qk^T        -> out
+//   U~^T = V^T T^T (bf16 hi + lo)
+//   hand-off (tf32):        replay:  P^T = S^T (k e^g)^T,  U^T = U~^T - P^T T^T
+//                           summary: W^T = (k e^g)^T T^T,  U^T = U~^T - S^T W^T
+//                           O^T = S^T (q e^g)^T + U^T A_qk^T        -> out (replay)
 //                           S^T <- S^T Diag(e^{g_last}) + U^T K',  K' = k e^{g_last - g}
 //
 // Tokens of a chunk are processed together and only the state is handed on
@@ -31,18 +32,19 @@
 // the output); T is fp32 and enters the tf32 MMA rounded to nearest, and the
 // bf16 MMA with V (exact in bf16) as a hi + lo pair of bf16; every operand on
 // the state path is tf32 rounded to nearest; accumulation is fp32.  tf32
-// operands are always laid out K-major: the key-side factors k e^g and K' are
-// written transposed, [key channel][token].
+// operands are always laid out K-major: K' (and, for W^T, k e^g) are written
+// transposed, [key channel][token]; k e^g for P^T and q e^g [token][channel].
 //
-// Schedule of chunk n (16 worker warps; two issuer threads in a control
-// warpgroup issue the MMAs and the TMA copies):
-//   A  strip MMA (n)                     || read O^T (n-1) out of TMEM -> out
-//   B  strip read-out, UT transform (in place), T to SMEM
-//   C  W^T, U~^T MMAs (n)                || K' (n) to SMEM
-//   D  -W and q e^g to SMEM
-//   E  U^T -= S^T W^T ; O^T = S^T (q e^g)^T || decay scan of chunk n+1
+// Schedule of chunk n in the replay (16 worker warps; two issuer threads in a
+// control warpgroup issue the MMAs and the TMA copies):
+//   A  strip MMA (n) ; P^T (n)           || read O^T (n-1) out of TMEM -> out
+//   B  strip read-out, UT transform (in place), T to SMEM; meanwhile -P^T
+//      rounded to tf32 in TMEM and q e^g to SMEM
+//   C  O^T = S^T (q e^g)^T ; U^T = U~^T - P^T T^T  || K' (n), decay scan of n+1
 //   F  decay the columns of S^T, round U^T to tf32 (in TMEM)
 //   G  O^T += U^T A_qk^T ; S^T += U^T K' || operands of chunk n+1 to SMEM
+// The summary runs C as W^T, U~^T || K', then D (-W to SMEM) and E (U^T -=
+// S^T W^T for both of its states || decay scan of n+1).
 // Raw q, k, log_alpha stream in by TMA one chunk ahead; v after step C.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -805,9 +807,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
   // ================= control warps: issue the MMA groups once their operands are ready.
   // Issuing a tcgen05.mma costs the issuing thread ~100 cycles, far more than
-  // the tensor pipe needs for these shapes, so the two independent MMA chains
-  // of groups 1-3 are issued by two threads in parallel (issuer 0 and 1,
-  // lane 0 of the two control warps).  Each issuer commits its own chain.
+  // the tensor pipe needs for these shapes, so the independent MMA chains of
+  // each group are issued by two threads in parallel (issuer 0 and 1, lane 0
+  // of the two control warps).  Each issuer commits its own chain.
   auto control = [&](int who) {
     // K-major SW128 operand, 8-row groups 1024 B apart: K step j of a
     // [blocks][rows][128 B] tile starts at block j / 4, byte (j % 4) * 32.  The
