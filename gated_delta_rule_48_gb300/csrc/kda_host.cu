@@ -137,25 +137,41 @@ extern "C" kda_status kda_chunk_fwd_host(const void* q, const void* k, const voi
   const char* hb = reinterpret_cast<const char*>(beta);
   char* ho = static_cast<char*>(out);
   kda_status st = KDA_OK;
+  // Rows [t0, t0 + len) of every sequence between the host tensor ([N][Tb]
+  // rows of rb bytes) and the slice buffer ([N][len] rows): one strided 2-D
+  // copy when the host pitch is within the copy engines' limit, else one copy
+  // per sequence.
+  auto copy_rows = [&](char* dev, const char* host_src, char* host_dst, const char* dev_src,
+                       int64_t rb, int64_t t0, int64_t len, cudaMemcpyKind kind,
+                       cudaStream_t st_) -> cudaError_t {
+    const size_t hp = static_cast<size_t>(Tb * rb), dp = static_cast<size_t>(len * rb);
+    if (hp < (size_t(1) << 31)) {
+      return kind == cudaMemcpyHostToDevice
+                 ? cudaMemcpy2DAsync(dev, dp, host_src + t0 * rb, hp, dp, N, kind, st_)
+                 : cudaMemcpy2DAsync(host_dst + t0 * rb, hp, dev_src, dp, dp, N, kind, st_);
+    }
+    for (int32_t n = 0; n < N; ++n) {
+      const int64_t h_row = n * Tb + t0, d_row = n * len;
+      const cudaError_t e =
+          kind == cudaMemcpyHostToDevice
+              ? cudaMemcpyAsync(dev + d_row * rb, host_src + h_row * rb, len * rb, kind, st_)
+              : cudaMemcpyAsync(host_dst + h_row * rb, dev_src + d_row * rb, len * rb, kind, st_);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  };
   for (int64_t i = 0; i < n_slices; ++i) {
     const int buf = static_cast<int>(i & 1);
     const int64_t t0 = i * L, len = (Tb - t0) < L ? (Tb - t0) : L;
     Set& B = set[buf];
     // inputs of slice i: the buffers' previous slice (i - 2) must have been computed
     if (i >= 2) KDA_TRY(cudaStreamWaitEvent(P.in, P.ev[2 + buf], 0));
-    for (int32_t n = 0; n < N; ++n) {
-      const int64_t src_row = n * Tb + t0, dst_row = n * len;
-      KDA_TRY(cudaMemcpyAsync(B.q + dst_row * qk_row, hq + src_row * qk_row, len * qk_row,
-                              cudaMemcpyHostToDevice, P.in));
-      KDA_TRY(cudaMemcpyAsync(B.k + dst_row * qk_row, hk + src_row * qk_row, len * qk_row,
-                              cudaMemcpyHostToDevice, P.in));
-      KDA_TRY(cudaMemcpyAsync(B.v + dst_row * v_row, hv + src_row * v_row, len * v_row,
-                              cudaMemcpyHostToDevice, P.in));
-      KDA_TRY(cudaMemcpyAsync(B.la + dst_row * la_row, hla + src_row * la_row, len * la_row,
-                              cudaMemcpyHostToDevice, P.in));
-      KDA_TRY(cudaMemcpyAsync(B.b + dst_row * b_row, hb + src_row * b_row, len * b_row,
-                              cudaMemcpyHostToDevice, P.in));
-    }
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    KDA_TRY(copy_rows(B.q, hq, nullptr, nullptr, qk_row, t0, len, h2d, P.in));
+    KDA_TRY(copy_rows(B.k, hk, nullptr, nullptr, qk_row, t0, len, h2d, P.in));
+    KDA_TRY(copy_rows(B.v, hv, nullptr, nullptr, v_row, t0, len, h2d, P.in));
+    KDA_TRY(copy_rows(B.la, hla, nullptr, nullptr, la_row, t0, len, h2d, P.in));
+    KDA_TRY(copy_rows(B.b, hb, nullptr, nullptr, b_row, t0, len, h2d, P.in));
     KDA_TRY(cudaEventRecord(P.ev[0 + buf], P.in));
     // prefill of slice i from the device state, in place
     KDA_TRY(cudaStreamWaitEvent(P.comp, P.ev[0 + buf], 0));
@@ -167,11 +183,7 @@ extern "C" kda_status kda_chunk_fwd_host(const void* q, const void* k, const voi
     KDA_TRY(cudaEventRecord(P.ev[2 + buf], P.comp));
     // outputs of slice i back to the host
     KDA_TRY(cudaStreamWaitEvent(P.out, P.ev[2 + buf], 0));
-    for (int32_t n = 0; n < N; ++n) {
-      const int64_t dst_row = n * Tb + t0, src_row = n * len;
-      KDA_TRY(cudaMemcpyAsync(ho + dst_row * v_row, B.o + src_row * v_row, len * v_row,
-                              cudaMemcpyDeviceToHost, P.out));
-    }
+    KDA_TRY(copy_rows(nullptr, nullptr, ho, B.o, v_row, t0, len, cudaMemcpyDeviceToHost, P.out));
     KDA_TRY(cudaEventRecord(P.ev[4 + buf], P.out));
   }
   if (S_final) {
