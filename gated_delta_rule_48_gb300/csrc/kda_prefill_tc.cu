@@ -90,13 +90,13 @@ constexpr uint32_t kR = kRawL + 32768;        // phase-dependent operand region 
 //   UT:       T tf32 [64][64] at +0, T_hi / T_lo bf16 [64][64] at +16384 / +24576,
 //             A_kk -> T' f32 [64][kLdA] at +32768, scratch 32 x 36 f32 after it
 //             (the transposed block A_(10) sits in the then idle K' buffer)
-//   hand-off: q e^g tf32 [64][128] at +0
-//   always:   A_qk tf32 [64][64] at +57344
+//   always:   A_qk tf32 [64][64] at +57344 (replay)
 constexpr uint32_t kLdA = 68;                 // padded row stride (floats)
-constexpr uint32_t kRT = 0, kRTh = 16384, kRTl = 24576, kRAkk = 32768, kRQ = 0;
+constexpr uint32_t kRT = 0, kRTh = 16384, kRTl = 24576, kRAkk = 32768;
 constexpr uint32_t kRAqk = 57344;
 constexpr uint32_t kRXs = kRAkk + C * kLdA * 4;  // UT scratch, 32 x 36 f32
-constexpr uint32_t kKG = kR + 73728;          // k e^g (transposed) -> -W  tf32
+constexpr uint32_t kKG = kR + 73728;          // k e^g tf32: replay [token][channel] -> q e^g;
+                                              // summary transposed -> -W
 constexpr uint32_t kKP = kKG + 32768;         // K' (transposed)            tf32
 constexpr uint32_t kMisc = kKP + 32768;
 // f32 warp totals [16][128] of the decay scan: live only in the first half of
@@ -920,100 +920,87 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         mma_commit(bar_done + 3);
         if (*s_abort) break;
       } else {  // summary: groups 0..3
-      for (int g = 0; g < 4; ++g) {
-        if (*s_abort) break;
-        const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
-        if (!ready) flag_timeout();
-        tc_fence_after();
-        const bool go = ready && !*s_abort;
-        if (g == 0) {
-          if (who == 0) {  // strip products (bf16)
-            if (go) {
-              const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
-              const uint64_t a0 = kdesc(R), b0 = kdesc(R + 32768);
-#pragma unroll 4
-              for (int j = 0; j < D / 16; ++j)
-                mma_f16_ss(tmem + cA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
+        for (int g = 0; g < 4; ++g) {
+          if (*s_abort) break;
+          const bool ready = mbar_wait(bar_ready + g, static_cast<uint32_t>(n & 1));
+          if (!ready) flag_timeout();
+          tc_fence_after();
+          const bool go = ready && !*s_abort;
+          if (g == 0) {
+            if (who == 0) {  // strip products (bf16)
+              if (go) {
+                const uint32_t id = make_idesc(kFmtBF16, 128, 96, false, false);
+                const uint64_t a0 = kdesc(R), b0 = kdesc(R + 32768);
+  #pragma unroll 4
+                for (int j = 0; j < D / 16; ++j)
+                  mma_f16_ss(tmem + cA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
+              }
+              mma_commit(bar_done + 0);
             }
-            mma_commit(bar_done + 0);
-          }
-        } else if (g == 1) {
-          if (who == 0) {  // W^T = (k e^g)^T T^T (tf32)
-            if (go) {
-              const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
-              const uint64_t kg = kdesc(KG), tt = kdesc(R + kRT);
-#pragma unroll 4
-              for (int j = 0; j < C / 8; ++j)
-                mma_tf32_ss(tmem + cW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
-            }
-          } else {  // U~^T = V^T T^T (bf16 hi + lo), once raw v has landed
-            bool ok = go;
-            if (ok && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
-            tc_fence_after();
-            if (ok) {
-              const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
-              const uint64_t vv = smem_desc_sw128(smem_u32(sm + kRawV), 64 * 128, 1024);
-              const uint64_t th = kdesc(R + kRTh), tl = kdesc(R + kRTl);
-#pragma unroll 4
-              for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
-                const int jj = j & 3;
-                mma_f16_ss(tmem + cU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
-                           idu, j > 0);
+          } else if (g == 1) {
+            if (who == 0) {  // W^T = (k e^g)^T T^T (tf32)
+              if (go) {
+                const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
+                const uint64_t kg = kdesc(KG), tt = kdesc(R + kRT);
+  #pragma unroll 4
+                for (int j = 0; j < C / 8; ++j)
+                  mma_tf32_ss(tmem + cW, kmaj(kg, j, 128 * 128), kmaj(tt, j, 64 * 128), idw, j > 0);
+              }
+            } else {  // U~^T = V^T T^T (bf16 hi + lo), once raw v has landed
+              bool ok = go;
+              if (ok && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+              tc_fence_after();
+              if (ok) {
+                const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
+                const uint64_t vv = smem_desc_sw128(smem_u32(sm + kRawV), 64 * 128, 1024);
+                const uint64_t th = kdesc(R + kRTh), tl = kdesc(R + kRTl);
+  #pragma unroll 4
+                for (int j = 0; j < 2 * (C / 16); ++j) {  // hi half (j < 4), then lo half
+                  const int jj = j & 3;
+                  mma_f16_ss(tmem + cU, vv + ((jj * 2048) >> 4), (j < 4 ? th : tl) + ((jj * 32) >> 4),
+                             idu, j > 0);
+                }
               }
             }
-          }
-          mma_commit(bar_done + 1);
-          // raw v of chunk n consumed once group 1 has completed: stream in n+1
-          if (who == 1 && n + 1 < n_chunks) {
-            if (mbar_wait(bar_done + 1, static_cast<uint32_t>(n & 1))) issue_v(sg.t0 + (n + 1) * C);
-            else flag_timeout();
-          }
-        } else if (g == 2) {
-          const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-          if (go && who == 0) {  // U^T -= S^T W^T (KG holds -W)
-            const uint64_t wm = kdesc(KG);
-#pragma unroll 4
-            for (int j = 0; j < D / 8; ++j)
-              mma_tf32_ts(tmem + cU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id, 1);
-          }
-          if (go && who == 1 && kSum) {  // U_M^T = -S_M^T W^T (no values)
-            const uint64_t wm = kdesc(KG);
-#pragma unroll 4
-            for (int j = 0; j < D / 8; ++j)
-              mma_tf32_ts(tmem + cUM, tmem + cSM + 8 * j, kmaj(wm, j, 64 * 128), id, j > 0);
-          }
-          if (go && who == 1 && kOut) {  // O^T = S^T (q e^g)^T
-            const uint64_t qg = kdesc(R + kRQ);
-#pragma unroll 4
-            for (int j = 0; j < D / 8; ++j)
-              mma_tf32_ts(tmem + kColO, tmem + kColS + 8 * j, kmaj(qg, j, 64 * 128), id, j > 0);
-          }
-          mma_commit(bar_done + 2);
-        } else {
-          if (go && who == 1 && kOut) {  // O^T += U^T A_qk^T
+            mma_commit(bar_done + 1);
+            // raw v of chunk n consumed once group 1 has completed: stream in n+1
+            if (who == 1 && n + 1 < n_chunks) {
+              if (mbar_wait(bar_done + 1, static_cast<uint32_t>(n & 1))) issue_v(sg.t0 + (n + 1) * C);
+              else flag_timeout();
+            }
+          } else if (g == 2) {
             const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
-            const uint64_t aq = kdesc(R + kRAqk);
-#pragma unroll 4
-            for (int j = 0; j < C / 8; ++j)
-              mma_tf32_ts(tmem + kColO, tmem + cU + 8 * j, kmaj(aq, j, 64 * 128), id, 1);
+            if (go && who == 0) {  // U^T -= S^T W^T (KG holds -W)
+              const uint64_t wm = kdesc(KG);
+  #pragma unroll 4
+              for (int j = 0; j < D / 8; ++j)
+                mma_tf32_ts(tmem + cU, tmem + kColS + 8 * j, kmaj(wm, j, 64 * 128), id, 1);
+            }
+            if (go && who == 1) {  // U_M^T = -S_M^T W^T (no values)
+              const uint64_t wm = kdesc(KG);
+  #pragma unroll 4
+              for (int j = 0; j < D / 8; ++j)
+                mma_tf32_ts(tmem + cUM, tmem + cSM + 8 * j, kmaj(wm, j, 64 * 128), id, j > 0);
+            }
+            mma_commit(bar_done + 2);
+          } else {
+            if (go && who == 1) {  // S_M^T += U_M^T K'
+              const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+              const uint64_t kp = kdesc(KP);
+  #pragma unroll 4
+              for (int j = 0; j < C / 8; ++j)
+                mma_tf32_ts(tmem + cSM, tmem + cUM + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
+            }
+            if (go && who == 0) {  // S^T += U^T K'
+              const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
+              const uint64_t kp = kdesc(KP);
+  #pragma unroll 4
+              for (int j = 0; j < C / 8; ++j)
+                mma_tf32_ts(tmem + kColS, tmem + cU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
+            }
+            mma_commit(bar_done + 3);
           }
-          if (go && who == 1 && kSum) {  // S_M^T += U_M^T K'
-            const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-            const uint64_t kp = kdesc(KP);
-#pragma unroll 4
-            for (int j = 0; j < C / 8; ++j)
-              mma_tf32_ts(tmem + cSM, tmem + cUM + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
-          }
-          if (go && who == 0) {  // S^T += U^T K'
-            const uint32_t ids = make_idesc(kFmtTF32, 128, 128, false, false);
-            const uint64_t kp = kdesc(KP);
-#pragma unroll 4
-            for (int j = 0; j < C / 8; ++j)
-              mma_tf32_ts(tmem + kColS, tmem + cU + 8 * j, kmaj(kp, j, 128 * 128), ids, 1);
-          }
-          mma_commit(bar_done + 3);
         }
-      }
       }
       if (*s_abort) break;
     }
