@@ -75,3 +75,32 @@ def test_concurrent_calls_on_two_streams():
     torch.cuda.synchronize()
     for (o, S), (ro, rS) in zip(outs, refs):
         assert torch.equal(o, ro) and torch.equal(S, rS)
+
+
+def test_decode_tokens_captured_in_a_cuda_graph():
+    """The persistent multi-token decode (with commit counts) inside a graph:
+    two replays from the same starting state equal the eager call bit for bit."""
+    dec = kin.make_decode(40, 4, 128, steps=5, seed=84)
+    f = lambda t: t.transpose(0, 1).contiguous().cuda()
+    q, k, v, la, b = f(dec.q), f(dec.k), f(dec.v), f(dec.log_alpha), f(dec.beta)
+    commit = torch.tensor([5, 0, 3, 1] * 10, dtype=torch.int32, device="cuda")
+    S_ref = dec.S.cuda()
+    ref_out = kb.kda_decode_tokens(q, k, v, la, b, S_ref, commit)
+    S_g = dec.S.cuda()
+    out = torch.empty_like(ref_out)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up on the capture stream
+        kb.kda_decode_tokens(q, k, v, la, b, S_g.clone(), commit, out, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kb.kda_decode_tokens(q, k, v, la, b, S_g, commit, out, stream=torch.cuda.current_stream())
+    for rep in range(2):
+        out.zero_()
+        S_g.copy_(dec.S.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert kb.kda_get_device_error() == 0
+        assert torch.equal(out, ref_out) and torch.equal(S_g, S_ref)
