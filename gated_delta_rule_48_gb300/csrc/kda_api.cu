@@ -250,9 +250,10 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   size_t off_nseg = 0;
   size_t off_segs = align_up(off_nseg + sizeof(int32_t));
   size_t off_it = align_up(off_segs + sizeof(Segment) * capacity);
-  size_t it_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)(dv + dk) : 0;
+  // (B | M) records and entry states at the kernels' state width
+  size_t it_bytes = split ? sizeof(float) * capacity * H * kStateD * (size_t)(2 * kStateD) : 0;
   size_t off_es = align_up(off_it + it_bytes);
-  size_t es_bytes = split ? sizeof(float) * capacity * H * dk * (size_t)dv : 0;
+  size_t es_bytes = split ? sizeof(float) * capacity * H * kStateD * (size_t)kStateD : 0;
   const bool want_ckpt = ckpt_interval > 0;  // the planner counts (and flags an overflow) even if max = 0
   size_t off_ck = align_up(off_es + es_bytes);
   size_t ck_base_bytes = want_ckpt ? sizeof(int64_t) * (size_t)N : 0;

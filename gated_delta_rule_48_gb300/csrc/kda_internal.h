@@ -10,6 +10,8 @@
 namespace kda {
 
 constexpr int kChunk = 64;      // tokens per chunk
+constexpr int kStateD = 128;    // width of the chunk kernels' states: d = 64 runs
+                                // zero-padded to 128 (exact: see kda_prefill_tc.cu)
 constexpr int kSubTile = 16;    // tokens per decay tile inside a chunk
 constexpr float kLogAlphaMin = -5.0f;
 
@@ -85,11 +87,9 @@ cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 
 // ---- chunked prefill (kda_prefill_*.cu)
 // pass 0: summary (B_j, M_j) of every non-final segment; pass 1: replay.
+// tcgen05 kernels (kda_prefill_tc.cu), dk = dv = 128 or 64
 cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
-// tcgen05 kernels (dk = dv = 128), kda_prefill_tc.cu
-cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s);
-cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s);
 
 // ---- decode (kda_decode.cu)
 struct DecodeArgs {

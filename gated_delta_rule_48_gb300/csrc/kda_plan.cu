@@ -157,21 +157,26 @@ segment_scan_kernel(PrefillArgs a) {
   }
   __syncthreads();
   if (s_first < 0 || s_count <= 1) return;
-  const int W = a.dv + D;  // width of the B | M record
+  // records and entry states are D (128) wide; the caller's S0 is a.dv wide
+  // (64 runs zero-padded to 128)
+  const int W = 2 * D;  // width of the B | M record
+  const int DIO = a.dv;
   auto rec_of = [&](int64_t seg) {
     return a.incr_trans + (seg * a.H + h) * static_cast<int64_t>(D) * W;
   };
   auto stage_M = [&](int buf, const float* rec) {  // M_j -> sm.M[buf], 16 bytes per copy
     for (int i = tid; i < D * (D / 4); i += kScanThreads) {
       const int c = i / (D / 4), m4 = i % (D / 4);
-      cp_async16(&sm.M[buf][c * LD + 4 * m4], rec + static_cast<int64_t>(c) * W + a.dv + 4 * m4);
+      cp_async16(&sm.M[buf][c * LD + 4 * m4], rec + static_cast<int64_t>(c) * W + D + 4 * m4);
     }
     cp_async_commit();
   };
   stage_M(0, rec_of(s_first));
   for (int i = tid; i < D * kScanCols; i += kScanThreads) {
     const int c = i / kScanCols, j = i % kScanCols;
-    sm.S[i] = a.S0 ? a.S0[((static_cast<int64_t>(n) * a.H + h) * D + c) * a.dv + col0 + j] : 0.f;
+    sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO)
+                  ? a.S0[((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j]
+                  : 0.f;
   }
   const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + 32 r
   for (int sgi = 0; sgi + 1 < s_count; ++sgi) {
@@ -199,8 +204,8 @@ segment_scan_kernel(PrefillArgs a) {
     for (int r = 0; r < RPT; ++r) {
       const int c = c0 + 32 * r;
       sm.S[c * kScanCols + j] = acc[r];
-      a.entry_state[((seg + 1) * a.H + h) * static_cast<int64_t>(D) * a.dv +
-                    static_cast<int64_t>(c) * a.dv + col0 + j] = acc[r];
+      a.entry_state[((seg + 1) * a.H + h) * static_cast<int64_t>(D) * D +
+                    static_cast<int64_t>(c) * D + col0 + j] = acc[r];
     }
     __syncthreads();
   }
@@ -217,20 +222,14 @@ cudaError_t launch_plan(const int32_t* cu_seqlens, int64_t T, int32_t N, int64_t
 }
 
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s) {
-  dim3 grid(a.N, a.H, a.dv / kScanCols);
+  // the chunk kernels keep 128-wide states for both head sizes
+  dim3 grid(a.N, a.H, kStateD / kScanCols);
   prof_begin(s, "kda_segment_scan");
-  cudaError_t e;
-  if (a.dk == 128) {
-    e = cudaFuncSetAttribute(segment_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(ScanSmem<128>)));
-    if (e == cudaSuccess)
-      segment_scan_kernel<128><<<grid, kScanThreads, sizeof(ScanSmem<128>), s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(segment_scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(ScanSmem<64>)));
-    if (e == cudaSuccess)
-      segment_scan_kernel<64><<<grid, kScanThreads, sizeof(ScanSmem<64>), s>>>(a);
-  }
+  cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel<kStateD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(ScanSmem<kStateD>)));
+  if (e == cudaSuccess)
+    segment_scan_kernel<kStateD><<<grid, kScanThreads, sizeof(ScanSmem<kStateD>), s>>>(a);
   prof_end(s, "kda_segment_scan");
   return e != cudaSuccess ? e : cudaGetLastError();
 }

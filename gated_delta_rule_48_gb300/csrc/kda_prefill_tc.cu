@@ -1,4 +1,5 @@
-// Chunk-parallel prefill on the tcgen05 tensor cores (dk = dv = 128).
+// Chunk-parallel prefill on the tcgen05 tensor cores (dk = dv = 128; 64 runs
+// zero-padded to 128).
 //
 // One CTA per unit = (segment, head) walks the segment's 64-token chunks in
 // order.  The state is kept TRANSPOSED in tensor memory
@@ -430,6 +431,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   // only the state-reading products and the state updates are doubled.
   constexpr bool kOut = MODE == kModeReplay;
   constexpr bool kSum = MODE == kModeSummary;
+  // Width of the caller's tensors: 128, or 64 run zero-padded to 128 (the
+  // maps read channels >= 64 as zeros; zero key and query channels add
+  // nothing, and zero value channels stay zero, so the 64 x 64 block is
+  // exact).  Internal records (B | M, entry states) are always 128 wide.
+  const int DIO = a.dv;
   // TMEM columns of this mode.  Replay: S^T 0, strip products 128, W^T 256,
   // U^T 320, O^T 384.  Summary: S_B^T 0, S_M^T 128, U_B^T 256, U_M^T 320, and
   // the strip products share 384.. with W^T: W^T of chunk n is read out (phase
@@ -546,17 +552,18 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     const float* src = nullptr;
     if (MODE == kModeReplay) {
       if (sg.index == 0)
-        src = a.S0 ? a.S0 + (static_cast<int64_t>(sg.seq) * H + h) * D * D : nullptr;
+        src = a.S0 ? a.S0 + (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO : nullptr;
       else
         src = a.entry_state + (static_cast<int64_t>(seg_id) * H + h) * D * D;
     }
+    const int lds = (MODE == kModeReplay && sg.index == 0) ? DIO : D;  // row stride of src
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
       uint32_t r[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         const int c = 32 * part + cc + x;
-        r[x] = __float_as_uint(src ? src[c * D + j] : 0.f);
+        r[x] = __float_as_uint(src && c < lds && j < lds ? src[c * lds + j] : 0.f);
       }
       tmem_st16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), r);
       if (kSum) {  // S_M = I
@@ -733,21 +740,24 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
       const int t = 16 * part + 2 * y + (odd ? 1 : 0);
       const float lo = odd ? recv : v0, hi = odd ? v1 : recv;
-      if (t < valid)
-        *reinterpret_cast<uint32_t*>(a.out + ((c0 + t) * H + h) * D + (j & ~1)) = pack_bf16x2(lo, hi);
+      if (t < valid && j < DIO)
+        *reinterpret_cast<uint32_t*>(a.out + ((c0 + t) * H + h) * DIO + (j & ~1)) = pack_bf16x2(lo, hi);
     }
   };
 
   // S^T (TMEM) -> dst[c * ld + j] = S[c][j] (row = key channel), f32; worker warps.
-  auto store_state = [&](float* dst, int64_t ld, uint32_t col) {
+  // rows and columns below lim of the state in TMEM columns col.. to dst
+  auto store_state = [&](float* dst, int64_t ld, uint32_t col, int lim) {
     const int j = 32 * quad + lane;
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
       uint32_t sv[16];
       tmem_ld16(tmem_addr(tmem, 32 * quad, col + 32 * part + cc), sv);
       tmem_wait_ld();
+      if (j < lim && 32 * part + cc < lim) {
 #pragma unroll
-      for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+        for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+      }
     }
   };
   // Phase F on one state: decay the columns of S^T (TMEM columns cs..) by
@@ -1165,15 +1175,18 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         if (pos % ci == 0) {
           const int64_t slot = a.plan.ckpt_base[sg.seq] + pos / ci - 1;
           if (slot < a.plan.ckpt_max) {  // 8 columns at a time: few live registers mid-loop
-            float* dst = a.ckpt + (slot * H + h) * D * D;
+            float* dst = a.ckpt + (slot * H + h) * DIO * DIO;
             const int j = 32 * quad + lane;
 #pragma unroll 1
             for (int cc = 0; cc < 32; cc += 8) {
               uint32_t sv[16];
               tmem_ld8(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), sv);
               tmem_wait_ld();
+              if (j < DIO && 32 * part + cc < DIO) {
 #pragma unroll
-              for (int x = 0; x < 8; ++x) dst[(32 * part + cc + x) * D + j] = __uint_as_float(sv[x]);
+                for (int x = 0; x < 8; ++x)
+                  dst[(32 * part + cc + x) * DIO + j] = __uint_as_float(sv[x]);
+              }
             }
           }
         }
@@ -1186,11 +1199,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     if (!*s_abort) {
       if (MODE == kModeReplay) {
         if (last && a.S_final)
-          store_state(a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * D * D, D, kColS);
+          store_state(a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO, DIO, kColS, DIO);
       } else {  // the increment | transition record, rows of 2 D floats
         float* dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D);
-        store_state(dst, 2 * D, kColS);
-        store_state(dst + D, 2 * D, cSM);
+        store_state(dst, 2 * D, kColS, D);
+        store_state(dst + D, 2 * D, cSM, D);
       }
     }
   }  // worker warps
@@ -1224,13 +1237,13 @@ EncodeTiledFn encode_fn() {
 // [T][H][128] tensor viewed as 3-D (channel, head, token); box = box_c channels
 // x 1 head x 64 tokens, 128-byte swizzle.  Rows past T read as zero.
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int64_t T,
-              int H, uint32_t box_c) {
+              int H, int dch, uint32_t box_c) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(dch), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(T)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esize,
-                                 static_cast<cuuint64_t>(H) * D * esize};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(dch) * esize,
+                                 static_cast<cuuint64_t>(H) * dch * esize};
   const cuuint32_t box[3] = {box_c, 1, static_cast<cuuint32_t>(C)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -1244,12 +1257,14 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   TcMaps maps;
   memset(&maps, 0, sizeof maps);
   if (a.T > 0) {
-    const bool ok = make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
-                    make_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
-                    make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) &&
-                    (FUSED ? make_map(&maps.la, a.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64)
-                           : make_map(&maps.la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T,
-                                      a.H, 32));
+    const int dch = a.dv;  // 64: the boxes past channel 63 read as zeros
+    const bool ok =
+        make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, dch, 64) &&
+        make_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, dch, 64) &&
+        make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, dch, 64) &&
+        (FUSED ? make_map(&maps.la, a.gate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, dch, 64)
+               : make_map(&maps.la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, dch,
+                          32));
     if (!ok) return cudaErrorInvalidValue;
   }
   // The register split inside the kernel assumes the launch allocation; a
@@ -1276,12 +1291,12 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
 
 }  // namespace
 
-cudaError_t launch_prefill_summary_tc(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s) {
   return a.fused ? launch_tc<kModeSummary, true, false>(a, s, "kda_prefill_summary")
                  : launch_tc<kModeSummary, false, false>(a, s, "kda_prefill_summary");
 }
 
-cudaError_t launch_prefill_replay_tc(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s) {
   if (a.ckpt)
     return a.fused ? launch_tc<kModeReplay, true, true>(a, s, "kda_prefill_replay")
                    : launch_tc<kModeReplay, false, true>(a, s, "kda_prefill_replay");
