@@ -17,11 +17,11 @@
 // tokens, written back once: the speculative-decoding verify / commit form of
 // the orkas.ai close read, section "The bill comes due in the serving stack").
 //
-// Persistent: two CTAs of 2D threads per SM, each walking (sequence, head)
-// units with a stride of the grid.  While a unit is computed from registers,
-// the next unit's state (64 KiB at D = 128) streams into shared memory by one
-// bulk asynchronous copy, so its HBM read overlaps the arithmetic; the
-// committed state goes from registers straight to HBM.
+// Persistent: two (D = 128) or four (D = 64) CTAs of 2D threads per SM, each
+// walking (sequence, head) units with a stride of the grid.  While a unit is
+// computed from registers, the next unit's state (64 KiB at D = 128) streams
+// into shared memory by one bulk asynchronous copy, so its HBM read overlaps
+// the arithmetic; the committed state goes from registers straight to HBM.
 //
 // Thread (p, quarter) owns the state columns j = 2p, 2p + 1 over rows
 // [quarter D/4, quarter D/4 + D/4).  A warp holds one quarter (D/64 warps
@@ -112,6 +112,7 @@ __device__ __forceinline__ void load_f32(const float* p, float (&f)[PER]) {
 template <int D>
 struct TokCfg {
   static constexpr int kThreads = 2 * D;
+  static constexpr int kCtasPerSm = D == 128 ? 2 : 4;  // 64 KiB | 16 KiB of state each
   static constexpr int kWarps = kThreads / 32;
   static constexpr int kRows = D / 4;   // state rows per thread (2 columns each)
   static constexpr int kWarpsPerQuarter = D / 64;
@@ -124,7 +125,7 @@ struct TokCfg {
 };
 
 template <int D, bool FUSED>
-__global__ void __launch_bounds__(TokCfg<D>::kThreads, 2)
+__global__ void __launch_bounds__(TokCfg<D>::kThreads, TokCfg<D>::kCtasPerSm)
 decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                      const uint16_t* __restrict__ v, const float* __restrict__ log_alpha,
                      const uint16_t* __restrict__ gate, const float* __restrict__ beta,
@@ -361,7 +362,8 @@ cudaError_t launch_t(const DecodeArgs& a, int64_t units, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(TokCfg<D>::kSmem));
   if (e != cudaSuccess) return e;
-  const int64_t grid = units < 2LL * sms[dev] ? units : 2LL * sms[dev];
+  const int64_t per_wave = static_cast<int64_t>(TokCfg<D>::kCtasPerSm) * sms[dev];
+  const int64_t grid = units < per_wave ? units : per_wave;
   kern<<<static_cast<unsigned>(grid), TokCfg<D>::kThreads, TokCfg<D>::kSmem, s>>>(
       a.q, a.k, a.v, a.log_alpha, a.gate, a.beta, a.S, a.out, a.commit, a.K, a.H, units, a.err);
   return cudaGetLastError();
