@@ -121,6 +121,8 @@ def load():
             lib.kda_last_error_message.restype = ctypes.c_char_p
             lib.kda_last_error_message.argtypes = []
             lib.kda_abi_version.restype = ctypes.c_int
+            lib.kda_selftest_bounded_wait.restype = ctypes.c_int
+            lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
             lib.kda_profile_enable.restype = None
             lib.kda_profile_enable.argtypes = [ctypes.c_int]
             lib.kda_profile_read.restype = ctypes.c_int
@@ -253,6 +255,12 @@ def kda_decode_step_fused(q_raw, k_raw, v, gate, beta, S_inout, out=None, *, str
 def kda_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return load().kda_get_device_error(_stream(stream))
+
+
+def kda_selftest_bounded_wait(polls: int = 1000, *, stream=None):
+    """One bounded wait on an mbarrier nothing arrives on (see include/kda.h);
+    the next kda_get_device_error() reports the timeout."""
+    _check(load().kda_selftest_bounded_wait(int(polls), _stream(stream)))
 
 
 def profile_enable(on: bool = True):

@@ -459,11 +459,24 @@ extern "C" kda_status kda_get_device_error(void* stream) {
   if (word & kDevErrCuSeqlens)
     msg += "cu_seqlens is malformed (cu[0] != 0, decreasing, or cu[N] != total_tokens); ";
   if (word & kDevErrCapacity) msg += "segment plan exceeded its workspace; ";
-  if (word & kDevErrTimeout) msg += "a prefill kernel timed out waiting for its tensor-core work; ";
+  if (word & kDevErrTimeout)
+    msg += "a kernel timed out waiting for its asynchronous copies or tensor-core work; ";
   if (word & kDevErrCommit) msg += "a decode commit count is outside [0, n_tokens]; ";
   if (word & kDevErrCheckpoints)
     msg += "the sequences have more checkpoints than max_checkpoints (the excess was dropped); ";
   return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
+}
+
+extern "C" kda_status kda_selftest_bounded_wait(uint32_t polls, void* stream) {
+  if (polls == 0 || polls > (1u << 20))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "polls must be in [1, 2^20] (got %u)", polls);
+  DeviceState* dev = nullptr;
+  kda_status st = device_state(&dev);
+  if (st != KDA_OK) return st;
+  const cudaError_t e =
+      launch_bounded_wait_selftest(polls, dev->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return KDA_OK;
 }
 
 extern "C" const char* kda_status_string(kda_status status) {

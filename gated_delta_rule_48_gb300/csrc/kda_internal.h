@@ -108,6 +108,8 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 // K > 1 tokens per sequence (kda_decode_tokens.cu); launch_decode dispatches to it
 cudaError_t launch_decode_tokens(const DecodeArgs& a, cudaStream_t s);
+// kda_selftest.cu: a bounded wait on an mbarrier nothing arrives on
+cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, cudaStream_t s);
 
 // bf16 helpers usable from device code without cuda_bf16.h conversions.
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {

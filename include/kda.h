@@ -349,6 +349,19 @@ const char *kda_last_error_message(void);
 int kda_abi_version(void);
 
 /*
+ * kda_selftest_bounded_wait -- launch, on `stream`, one wait of the kind every
+ * kernel of the library makes on its own asynchronous copies and tensor-core
+ * work, on an mbarrier that nothing ever arrives on.  The wait gives up after
+ * `polls` polls (each blocks for a hardware-chosen interval, so 1000 polls end
+ * within milliseconds) and records a timeout in the device error word, which
+ * the next kda_get_device_error(stream) returns as KDA_ERR_DEVICE_INPUT with
+ * a message naming the timeout.  Shows that a kernel whose work never arrives
+ * reports it instead of hanging, and that the context stays usable.
+ * polls in [1, 2^20], else KDA_ERR_INVALID_ARGUMENT.
+ */
+kda_status kda_selftest_bounded_wait(uint32_t polls, void *stream);
+
+/*
  * Launch timing (tracing aid).  While enabled, every kernel the library
  * launches is bracketed by CUDA events on its launch stream.
  * kda_profile_read() synchronises the device, then reports per kernel name

@@ -189,3 +189,9 @@ def test_host_api_validates_arguments(lib):
     assert lib.kda_chunk_fwd_host(*a, 96, 3, 2, 96, 96, 0, None) == UNSUPPORTED
     assert lib.kda_chunk_fwd_host(None, *a[1:], 96, 3, 2, 64, 64, 0, None) == INVALID
     assert lib.kda_chunk_fwd_host(*a, 0, 0, 2, 64, 64, 0, None) == OK
+
+
+def test_selftest_rejects_bad_poll_counts(lib):
+    # host-side checks only: nothing is launched
+    assert lib.kda_selftest_bounded_wait(0, None) == 1  # KDA_ERR_INVALID_ARGUMENT
+    assert lib.kda_selftest_bounded_wait((1 << 20) + 1, None) == 1
