@@ -259,16 +259,22 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   size_t ck_base_bytes = want_ckpt ? sizeof(int64_t) * (size_t)N : 0;
   size_t ws_bytes = align_up(off_ck + ck_base_bytes);
 
+  // A uniform batch with neither split nor checkpoints needs no plan and no
+  // workspace: the chunk kernel takes segment i = sequence i.
+  const bool direct = !cu_seqlens && !split && !want_ckpt && T > 0;
   char* ws = nullptr;
-  // Stream capture turns the allocation into a graph memory node, which takes
-  // the default pool; otherwise the library's own pool keeps workspace cached.
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(s, &cap);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-  e = cap == cudaStreamCaptureStatusNone
-          ? cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s)
-          : cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  cudaError_t e = cudaSuccess;
+  if (!direct) {
+    // Stream capture turns the allocation into a graph memory node, which takes
+    // the default pool; otherwise the library's own pool keeps workspace cached.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    e = cap == cudaStreamCaptureStatusNone
+            ? cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s)
+            : cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  }
 
   PrefillArgs a;
   a.q = static_cast<const uint16_t*>(q);
@@ -284,9 +290,10 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.T = T; a.N = N; a.H = H; a.dk = dk; a.dv = dv;
   a.incr_trans = split ? reinterpret_cast<float*>(ws + off_it) : nullptr;
   a.entry_state = split ? reinterpret_cast<float*>(ws + off_es) : nullptr;
-  a.plan.segs = reinterpret_cast<Segment*>(ws + off_segs);
-  a.plan.n_segs = reinterpret_cast<int32_t*>(ws + off_nseg);
+  a.plan.segs = direct ? nullptr : reinterpret_cast<Segment*>(ws + off_segs);
+  a.plan.n_segs = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_nseg);
   a.plan.capacity = capacity;
+  if (direct) a.plan.direct_len = T / N;
   if (want_ckpt) {
     a.plan.ckpt_base = reinterpret_cast<int64_t*>(ws + off_ck);
     a.plan.ckpt_interval = ckpt_interval;
@@ -296,13 +303,15 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.err = dev->err;
 
   kda_status result = KDA_OK;
-  e = launch_plan(cu_seqlens, T, N, L, a.plan, a.err, s);
+  if (!direct) e = launch_plan(cu_seqlens, T, N, L, a.plan, a.err, s);
   if (e == cudaSuccess && split) e = launch_prefill_summary(a, s);
   if (e == cudaSuccess && split) e = launch_segment_scan(a, s);
   if (e == cudaSuccess) e = launch_prefill_replay(a, s);
   if (e != cudaSuccess) result = cuda_fail(e, "prefill launch");
-  cudaError_t ef = cudaFreeAsync(ws, s);
-  if (result == KDA_OK && ef != cudaSuccess) result = cuda_fail(ef, "workspace free");
+  if (ws) {
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (result == KDA_OK && ef != cudaSuccess) result = cuda_fail(ef, "workspace free");
+  }
   return result;
 }
 

@@ -45,6 +45,9 @@ struct Plan {
   int64_t* ckpt_base = nullptr;  // [N], written by the planner
   int64_t ckpt_interval = 0;
   int64_t ckpt_max = 0;
+  // > 0: a uniform batch with neither split nor checkpoints, launched without
+  // the planner -- segment i is sequence i, direct_len tokens long
+  int64_t direct_len = 0;
 };
 
 // Problem description shared by the prefill kernels.

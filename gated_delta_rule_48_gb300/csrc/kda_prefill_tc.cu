@@ -421,8 +421,19 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t seg_id = blockIdx.x;
   const int h = blockIdx.y;
-  if (seg_id >= *a.plan.n_segs) return;
-  const Segment sg = a.plan.segs[seg_id];
+  Segment sg;
+  if (a.plan.direct_len > 0) {  // uniform batch, no planner: segment = sequence
+    if (seg_id >= a.N) return;
+    sg.t0 = static_cast<int64_t>(seg_id) * a.plan.direct_len;
+    sg.t1 = sg.t0 + a.plan.direct_len;
+    sg.seq = seg_id;
+    sg.index = 0;
+    sg.count = 1;
+    sg.first = seg_id;
+  } else {
+    if (seg_id >= *a.plan.n_segs) return;
+    sg = a.plan.segs[seg_id];
+  }
   const bool last = sg.index + 1 == sg.count;
   if (MODE == kModeSummary && last) return;
   // A summary unit carries two states through the segment: the increment B
