@@ -100,13 +100,12 @@ constexpr uint32_t kKG = kR + 73728;          // k e^g tf32: replay [token][chan
                                               // summary transposed -> -W
 constexpr uint32_t kKP = kKG + 32768;         // K' (transposed)            tf32
 constexpr uint32_t kMisc = kKP + 32768;
-// f32 warp totals [16][128] of the decay scan: live only in the first half of
-// the operand build, inside the (then unused) strip-B operand area of R
+// f32 warp totals [16][128] of the decay scan, then their exclusive prefixes:
+// live only inside the scan, in a part of R that no operand uses then
 constexpr uint32_t kTot = kR + 40960;
-constexpr uint32_t kG0 = kMisc;              // anchors g_15, g_47, g_63 [128] each
+constexpr uint32_t kG0 = kMisc;              // strip anchors g_15, g_47 [128] each
 constexpr uint32_t kG1 = kG0 + 512;
-constexpr uint32_t kGl = kG1 + 512;
-constexpr uint32_t kEGl = kGl + 512;          // e^{g_last} [2][128], by chunk parity
+constexpr uint32_t kEGl = kG1 + 512;          // e^{g_last} [2][128], by chunk parity
 constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e^{G0}, e^{G1},
                                               // e^{g_last - G0}, e^{g_last - G1}, e^{G1 - G0}
 constexpr uint32_t kBeta = kPC + 5 * 512;
@@ -475,7 +474,6 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   float* sTot = reinterpret_cast<float*>(sm + kTot);
   float* sG0 = reinterpret_cast<float*>(sm + kG0);
   float* sG1 = reinterpret_cast<float*>(sm + kG1);
-  float* sGl = reinterpret_cast<float*>(sm + kGl);
   float* sEGl = reinterpret_cast<float*>(sm + kEGl);
   float* sBeta = reinterpret_cast<float*>(sm + kBeta);
   unsigned char* R = sm + kR;
@@ -635,43 +633,41 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
     if (tid < C) sBeta[tid] = beta_reg;
     worker_sync();
+    if (warp < 4) {
+      // Across the 16 warps, lane = channel: the totals become exclusive
+      // prefixes in place (added in warp order, as a serial scan would), the
+      // anchors g_15, g_47, g_63 are the prefixes after warps 3, 11, 15, and
+      // the per-channel factors follow from them.
+      const int ch = 32 * warp + lane;
+      float acc = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float t = sTot[w * 128 + ch];
+        sTot[w * 128 + ch] = acc;
+        acc += t;
+        if (w == 3) a0 = acc;
+        if (w == 11) a1 = acc;
+      }
+      sG0[ch] = a0;
+      sG1[ch] = a1;
+      sEGl[(m & 1) * 128 + ch] = __expf(acc);
+      sPC[0 * 128 + ch] = __expf(a0);
+      sPC[1 * 128 + ch] = __expf(a1);
+      sPC[2 * 128 + ch] = __expf(acc - a0);
+      sPC[3 * 128 + ch] = __expf(acc - a1);
+      sPC[4 * 128 + ch] = __expf(a1 - a0);
+    }
     if (tid < C) {
       const int64_t t = sg.t0 + (m + 1) * C + tid;
       beta_reg = t < sg.t1 ? a.beta[t * H + h] : 0.f;
     }
-    {
-      float off[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w = 0; w < warp; ++w) {
-        const float4 t4 = *reinterpret_cast<const float4*>(sTot + w * 128 + 4 * lane);
-        off[0] += t4.x; off[1] += t4.y; off[2] += t4.z; off[3] += t4.w;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) g[i][x] += off[x];
-      // anchors: token 15 (warp 3), token 47 (warp 11), last token 63 (warp 15)
-      float* dst = warp == 3 ? sG0 : warp == 11 ? sG1 : warp == 15 ? sGl : nullptr;
-      if (dst)
-        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(g[3][0], g[3][1], g[3][2], g[3][3]);
-    }
     worker_sync();
-    if (warp == 0) {  // per-channel factors, once per chunk
-      const float4 g0 = *reinterpret_cast<const float4*>(sG0 + 4 * lane);
-      const float4 g1 = *reinterpret_cast<const float4*>(sG1 + 4 * lane);
-      const float4 gl = *reinterpret_cast<const float4*>(sGl + 4 * lane);
-      float* egl = sEGl + (m & 1) * 128;
-      *reinterpret_cast<float4*>(egl + 4 * lane) =
-          make_float4(__expf(gl.x), __expf(gl.y), __expf(gl.z), __expf(gl.w));
-      *reinterpret_cast<float4*>(sPC + 0 * 128 + 4 * lane) =
-          make_float4(__expf(g0.x), __expf(g0.y), __expf(g0.z), __expf(g0.w));
-      *reinterpret_cast<float4*>(sPC + 1 * 128 + 4 * lane) =
-          make_float4(__expf(g1.x), __expf(g1.y), __expf(g1.z), __expf(g1.w));
-      *reinterpret_cast<float4*>(sPC + 2 * 128 + 4 * lane) = make_float4(
-          __expf(gl.x - g0.x), __expf(gl.y - g0.y), __expf(gl.z - g0.z), __expf(gl.w - g0.w));
-      *reinterpret_cast<float4*>(sPC + 3 * 128 + 4 * lane) = make_float4(
-          __expf(gl.x - g1.x), __expf(gl.y - g1.y), __expf(gl.z - g1.z), __expf(gl.w - g1.w));
-      *reinterpret_cast<float4*>(sPC + 4 * 128 + 4 * lane) = make_float4(
-          __expf(g1.x - g0.x), __expf(g1.y - g0.y), __expf(g1.z - g0.z), __expf(g1.w - g0.w));
+    {
+      const float4 off = *reinterpret_cast<const float4*>(sTot + warp * 128 + 4 * lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        g[i][0] += off.x; g[i][1] += off.y; g[i][2] += off.z; g[i][3] += off.w;
+      }
     }
     {
       const float4 gA = *reinterpret_cast<const float4*>((strip ? sG1 : sG0) + 4 * lane);
