@@ -99,10 +99,12 @@ typedef enum {
  * A uniform batch [B, T_b, H, d] is passed as T = B * T_b, N = B,
  * cu_seqlens = NULL.  T = 0 or N = 0 is a valid no-op (S_final = S0).
  *
- * Memory: allocates a temporary workspace stream-ordered on `stream` and
- * frees it there: the segment plan (32 bytes per segment) and, when sequences
- * are split, (N + T / segment) * H * dk * (2 dv + dk) * 4 bytes of segment
- * summaries and entry states.
+ * Memory: a uniform batch (cu_seqlens = NULL) whose sequences are not split
+ * allocates nothing and is one kernel launch.  Otherwise the call allocates a
+ * temporary workspace stream-ordered on `stream` and frees it there: the
+ * segment plan (32 bytes per segment) and, when sequences are split,
+ * (N + T / segment) * H * dk * (2 dv + dk) * 4 bytes of segment summaries and
+ * entry states.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta,
