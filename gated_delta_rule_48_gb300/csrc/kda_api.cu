@@ -179,6 +179,8 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                 (long long)T, N, H);
   kda_status st = check_head_dims(dk, dv);
   if (st != KDA_OK) return st;
+  if (H > kMaxPrefillHeads)  // heads are the second grid dimension of the prefill kernels
+    return fail(KDA_ERR_UNSUPPORTED, "n_heads=%d exceeds %d", H, kMaxPrefillHeads);
   if (N == 0 && T > 0) return fail(KDA_ERR_INVALID_ARGUMENT, "tokens given but n_seqs = 0");
   if (!cu_seqlens && N > 0 && T % N != 0)
     return fail(KDA_ERR_INVALID_ARGUMENT,

@@ -64,6 +64,8 @@ extern "C" kda_status kda_chunk_fwd_host(const void* q, const void* k, const voi
   const int64_t T = total_tokens;
   const int32_t N = n_seqs;
   if (T < 0 || N < 0 || H <= 0) return report_error(KDA_ERR_INVALID_ARGUMENT, "bad sizes");
+  if (H > kMaxPrefillHeads)
+    return report_error(KDA_ERR_UNSUPPORTED, "n_heads exceeds 65535 (the prefill grid's second dimension)");
   if ((dk != 64 && dk != 128) || dv != dk)
     return report_error(KDA_ERR_UNSUPPORTED, "dk == dv in {64, 128} is required");
   if (N == 0 || T == 0) {

@@ -12,6 +12,8 @@ namespace kda {
 constexpr int kChunk = 64;      // tokens per chunk
 constexpr int kStateD = 128;    // width of the chunk kernels' states: d = 64 runs
                                 // zero-padded to 128 (exact: see kda_prefill_tc.cu)
+// The prefill kernels put heads on the grid's second dimension.
+constexpr int kMaxPrefillHeads = 65535;
 constexpr int kSubTile = 16;    // tokens per decay tile inside a chunk
 constexpr float kLogAlphaMin = -5.0f;
 

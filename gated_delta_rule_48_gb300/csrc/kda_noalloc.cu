@@ -81,6 +81,8 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const 
   // ---- host-side checks (same rules as kda_chunk_fwd), nothing launched on failure
   if (T < 0 || N < 0 || H <= 0)
     return report_error(KDA_ERR_INVALID_ARGUMENT, "total_tokens, n_seqs must be >= 0, n_heads > 0");
+  if (H > kMaxPrefillHeads)
+    return report_error(KDA_ERR_UNSUPPORTED, "n_heads exceeds 65535 (the prefill grid's second dimension)");
   if (dk <= 0 || dv <= 0) return report_error(KDA_ERR_INVALID_ARGUMENT, "dk and dv must be positive");
   if (dk != dv || (dk != 64 && dk != 128))
     return report_error(KDA_ERR_UNSUPPORTED, "only dk == dv in {64, 128} is supported");

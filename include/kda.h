@@ -24,7 +24,8 @@
  *   row-major (innermost index last, no padding) and 16-byte aligned.
  * - bf16 tensors are IEEE bfloat16; f32 tensors are IEEE binary32.
  * - Supported head sizes: dk == dv, and dk in {64, 128}.  Anything else
- *   returns KDA_ERR_UNSUPPORTED.
+ *   returns KDA_ERR_UNSUPPORTED.  The prefill entry points also take at most
+ *   65535 heads (n_heads); more return KDA_ERR_UNSUPPORTED.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every call is asynchronous with respect to the host and ordered
  *   on `stream`; calls on different streams may run concurrently.  The device

@@ -96,6 +96,17 @@ def test_prefill_rejects_bad_sizes(lib):
     assert prefill(lib, seg=100) == INVALID            # segment not a multiple of 64
 
 
+def test_prefill_rejects_more_heads_than_the_grid_allows(lib):
+    # heads are the prefill kernels' second grid dimension: at most 65535
+    assert prefill(lib, H=65536) == UNSUPPORTED
+    assert b"n_heads" in lib.kda_last_error_message()
+    a = [P(i) for i in range(9)]
+    a[6] = None  # uniform batch
+    assert lib.kda_chunk_fwd_noalloc(*a, 128, 2, 65536, 64, 64, None) == UNSUPPORTED
+    assert lib.kda_chunk_fwd_host(*[P(i) for i in range(8)], 96, 3, 65536, 64, 64, 0,
+                                  None) == UNSUPPORTED
+
+
 def test_prefill_rejects_overlaps(lib):
     assert prefill(lib, out=P(0, 64)) == INVALID          # out inside q
     assert b"out overlaps" in lib.kda_last_error_message()
