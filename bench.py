@@ -46,6 +46,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fused", action="store_true")
     ap.add_argument("--no-checkpoints", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long-context legs (workloads 2 and 3)")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="untimed seconds of the headline step with the clock sampler running")
     return ap.parse_args()
 
 
@@ -110,6 +114,23 @@ def recorded_traffic(kernel, src_file):
     if not os.path.exists(src) or rec.get("source_sha") != source_sha(src):
         return None
     return float(rec["bytes_per_launch"])
+
+
+def recorded_traffic_leg(kernel, workload_idx):
+    """DRAM bytes per launch of `kernel` on a long-context workload, from the
+    committed ncu summary, or None (absent, or another version of the source)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[f"{kernel}@w{workload_idx}"]
+    except (OSError, KeyError, ValueError):
+        return None
+    srcs = rec.get("sources", {})
+    for f, sha in srcs.items():
+        path = os.path.join(ROOT, "gated_delta_rule_48_gb300", "csrc", f)
+        if not os.path.exists(path) or source_sha(path) != sha:
+            return None
+    return float(rec["bytes_per_launch"]) if srcs else None
 
 
 # ---------------------------------------------------------------- clocks
@@ -221,10 +242,14 @@ def _device_inputs(p):
                 beta=p.beta.cuda(), S0=None if p.S0 is None else p.S0.cuda(), cu_seqlens=cu)
 
 
-def time_prefill(kb, p, steps, warmup, world):
+def time_prefill(kb, p, steps, warmup, world, soak_s=0.0, d=None):
     """Device-resident inputs; K timed kda_chunk_fwd calls bracketed by a
-    barrier and a synchronize.  Returns (ms per step, per-kernel tracing)."""
-    d = _device_inputs(p)
+    barrier and a synchronize.  Before them, ``soak_s`` seconds of the same
+    call run untimed with the clock sampler already on, so the clock record
+    covers a sustained load and not only the (short) timed region.  Returns
+    (ms per step, per-kernel tracing, clocks, per-step statistics)."""
+    if d is None:
+        d = _device_inputs(p)
     out = torch.empty((p.total_T, p.H, p.dv), dtype=torch.bfloat16, device="cuda")
     S = torch.empty((p.n_seqs, p.H, p.dk, p.dv), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -238,12 +263,19 @@ def time_prefill(kb, p, steps, warmup, world):
     if kb.kda_get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
     kb.profile_read()  # drop anything recorded so far
-    kb.profile_enable(True)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with ClockSampler(torch.cuda.current_device()) as clocks:
+        if soak_s > 0:
+            torch.cuda.synchronize()
+            t_end = time.perf_counter() + soak_s
+            while time.perf_counter() < t_end:
+                for _ in range(8):
+                    step()
+                torch.cuda.synchronize()
+        kb.profile_enable(True)
+        barrier(world)
+        torch.cuda.synchronize()
         start.record(stream)
         for i in range(steps):
             marks[i].record(stream)
@@ -258,6 +290,53 @@ def time_prefill(kb, p, steps, warmup, world):
     per = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(steps))
     stats = {"median": per[len(per) // 2], "min": per[0], "max": per[-1]}
     return ms, kernels, clocks.summary(), stats
+
+
+def long_leg(kb, idx, steps, warmup, world, peaks, peak_src):
+    """One long-context prefill workload (2 or 3) timed like the headline: the
+    whole kda_chunk_fwd call per step (planner, summary, scan and replay when
+    the library splits the sequences).  Inputs are drawn on the device with
+    the workload's recipe.  The roofline is that of the whole path: the
+    step's algorithmic bytes over the summed event time of the library's
+    kernels in one step."""
+    from gated_delta_rule_48_gb300 import inputs as kin
+    p = kin.workload_device(idx)
+    d = dict(q=p.q, k=p.k, v=p.v, log_alpha=p.log_alpha, beta=p.beta, S0=p.S0,
+             cu_seqlens=None if p.uniform else
+             torch.from_numpy(p.cu_seqlens.astype(np.int32)).cuda())
+    th, sh, dd = p.total_T * p.H, p.n_seqs * p.H, p.dk
+    alg_bytes = prefill_bytes(th, sh, dd, p.S0 is not None)
+    alg_flops = prefill_flops(th, dd)
+    ms, kernels, clocks, stats = time_prefill(kb, p, steps, warmup, world, d=d)
+    ms = max_over_ranks(ms, world)
+    path_ms = sum(t for _, t in kernels.values()) / steps
+    achieved = alg_bytes / (path_ms * 1e-3) / 1e9
+    top_name, (top_n, top_ms) = max(kernels.items(), key=lambda kv: kv[1][1])
+    tflops = alg_flops / (ms * 1e-3) / 1e12
+    attainable = min(peaks["bf16_tflops"], alg_flops / alg_bytes * peaks["hbm_gbs"] / 1e3)
+    traffic = None
+    recs = [recorded_traffic_leg(name, idx) for name in kernels]
+    if kernels and all(r is not None for r in recs):
+        traffic = sum(r * (n / steps) for r, (n, _) in zip(recs, kernels.values()))
+    leg = {
+        "workload": kin.WORKLOADS[idx], "value": p.total_T / (ms * 1e-3) / 1e6,
+        "unit": "Mtok/s", "ms_per_step": ms, "step_ms": stats,
+        "config": workload_config(p, idx),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "whole path: " + ", ".join(sorted(kernels)),
+                     "dominant_kernel": top_name, "peak_source": peak_src,
+                     "algorithmic_bytes_per_step": alg_bytes},
+        "tensor": {"tflops": tflops, "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+                   "attainable_tflops": attainable, "frac_of_attainable": tflops / attainable},
+        "kernels": {k: {"launches_per_step": n / steps, "avg_ms": t / n,
+                        "share": t / max(1e-12, sum(tt for _, tt in kernels.values()))}
+                    for k, (n, t) in kernels.items()},
+        "gpu_launches": sum(n for n, _ in kernels.values()),
+        "clocks": clocks,
+        "data": "synthetic, drawn on the device (same recipe and lengths, other values)",
+    }
+    return leg, p
 
 
 def time_prefill_fused(kb, r, steps, warmup):
@@ -457,6 +536,39 @@ def cpu_sample(p, n_seqs, max_tokens=None):
                 cu=cu, tokens=t1)
 
 
+def long_cpu_baseline(p, heads=(0, 2), max_tokens=65536):
+    """The oracle on heads 0-1 of the million-token workload, bounded to the
+    first `max_tokens` tokens of each sequence (16 independent chains)."""
+    import oracle
+    from gated_delta_rule_48_gb300 import inputs as kin
+    oracle.build()
+    threads = oracle.default_threads()
+    cu = p.cu_seqlens
+    rows, lens = [], []
+    for n in range(p.n_seqs):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        t1 = min(t1, t0 + max_tokens)
+        rows.append(torch.arange(t0, t1))
+        lens.append(t1 - t0)
+    idx = torch.cat(rows)
+    h0, h1 = heads
+    take = lambda t: t.index_select(0, idx.to(t.device))[:, h0:h1].contiguous().cpu()
+    q, k, v = take(p.q), take(p.k), take(p.v)
+    la, b = take(p.log_alpha), take(p.beta)
+    S0 = None if p.S0 is None else p.S0[:, h0:h1].contiguous().cpu().numpy()
+    cu_s = np.zeros(len(lens) + 1, dtype=np.int64)
+    cu_s[1:] = np.cumsum(lens)
+    sample = dict(q=kin.bf16_bits(q), k=kin.bf16_bits(k), v=kin.bf16_bits(v),
+                  log_alpha=la.numpy(), beta=b.numpy(), S0=S0, cu=cu_s, tokens=int(cu_s[-1]))
+    sec = time_oracle(sample, threads)
+    th = sample["tokens"] * (h1 - h0)
+    return {"value": th / sec / 1e6, "unit": "M token-heads/s", "cores": threads,
+            "kind": "oracle", "cpu": cpu_model(), "seconds": sec,
+            "sample": f"heads {h0}-{h1 - 1}, first {max_tokens} tokens of each of the "
+                      f"{p.n_seqs} sequences ({sample['tokens']} tokens, {th} token-heads), "
+                      "fp64 token-by-token recurrence"}
+
+
 def time_oracle(sample, threads):
     import oracle
     t0 = time.perf_counter()
@@ -548,7 +660,8 @@ def main():
     alg_bytes = prefill_bytes(th, sh, d, p.S0 is not None)
     alg_flops = prefill_flops(th, d)
 
-    ms, kernels, clocks, step_stats = time_prefill(kb, p, args.steps, args.warmup, world)
+    ms, kernels, clocks, step_stats = time_prefill(kb, p, args.steps, args.warmup, world,
+                                                   soak_s=args.soak_s)
     ms = max_over_ranks(ms, world)
     tokens_all = sum_over_ranks(p.total_T, world)
     value = tokens_all / (ms * 1e-3) / 1e6  # Mtok/s over all ranks
@@ -587,6 +700,20 @@ def main():
         "gpu_launches": launches,
         "clocks": clocks,
     }
+
+    if not args.no_long:
+        # the long-context workloads: 65,536-token sequences and the packed
+        # million-token batch, both split across SMs by the library
+        for idx in (2, 3):
+            if idx == args.workload:
+                continue
+            leg, lp = long_leg(kb, idx, max(3, min(args.steps, 20)), max(3, args.warmup),
+                               world, peaks, peak_src)
+            line[f"prefill_w{idx}"] = leg
+            if rank == 0 and world == 1 and not args.no_cpu_baseline and idx == 3:
+                leg["cpu_baseline"] = long_cpu_baseline(lp)
+            del lp
+            torch.cuda.empty_cache()
 
     if not args.no_e2e:
         e2e_fn = time_prefill_e2e_host if p.uniform else time_prefill_e2e

@@ -309,3 +309,72 @@ def make_decode_raw(N, H, dk, dv=None, steps=8, *, seed=5, s_std=0.02, name="") 
     return RawDecodeInputs(q_raw=p.q_raw.view(steps, N, H, dk), k_raw=p.k_raw.view(steps, N, H, dk),
                            v=p.v.view(steps, N, H, dv), gate=p.gate.view(steps, N, H, dk),
                            beta=p.beta.view(steps, N, H), S=S, name=name)
+
+
+# ---------------------------------------------------------------- device draws
+# The same recipe drawn directly on a CUDA device with torch's generator, for
+# timing runs of the large workloads: the shapes, sequence lengths, value
+# distributions and specials are those of :func:`workload`, the values are not
+# (a different random stream).  Parity tests use :func:`workload`.
+
+def _dev_normal(g, shape, device):
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
+
+def _dev_unit_bf16(g, T, H, d, device, block=_BLOCK):
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=device)
+    for t0 in range(0, T, block):
+        x = _dev_normal(g, (min(block, T - t0), H, d), device)
+        nrm = torch.linalg.vector_norm(x, dim=-1, keepdim=True).clamp_min(1e-12)
+        out[t0:t0 + x.shape[0]] = (x / nrm).to(torch.bfloat16)
+    return out
+
+
+def make_prefill_device(seq_lens, H, dk, dv=None, *, seed=0, s0_std=0.0,
+                        log_alpha_fixed=None, log_alpha_fixed_channels=None,
+                        beta_mode="sigmoid", name="", device="cuda") -> PrefillInputs:
+    """:func:`make_prefill`'s recipe drawn on ``device`` (tensors stay there)."""
+    dv = dk if dv is None else dv
+    seq_lens = [int(x) for x in seq_lens]
+    T = sum(seq_lens)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = _dev_unit_bf16(g, T, H, dk, device)
+    k = _dev_unit_bf16(g, T, H, dk, device)
+    v = torch.empty((T, H, dv), dtype=torch.bfloat16, device=device)
+    la = torch.empty((T, H, dk), dtype=torch.float32, device=device)
+    for t0 in range(0, T, _BLOCK):
+        n = min(_BLOCK, T - t0)
+        v[t0:t0 + n] = _dev_normal(g, (n, H, dv), device).to(torch.bfloat16)
+        la[t0:t0 + n] = -5.0 * torch.sigmoid(_dev_normal(g, (n, H, dk), device))
+    b = torch.sigmoid(_dev_normal(g, (T, H), device))
+    if log_alpha_fixed is not None:
+        sl = log_alpha_fixed_channels if log_alpha_fixed_channels is not None else slice(None)
+        la[:, :, sl] = float(log_alpha_fixed)
+    if beta_mode == "mix":
+        pick = torch.randint(0, 3, (T, H), generator=g, device=device)
+        b = torch.where(pick == 0, torch.zeros_like(b), torch.where(pick == 1, torch.ones_like(b), b))
+    elif beta_mode != "sigmoid":
+        raise ValueError(beta_mode)
+    N = len(seq_lens)
+    S0 = _dev_normal(g, (N, H, dk, dv), device) * s0_std if s0_std else None
+    cu = np.zeros(N + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(seq_lens)
+    return PrefillInputs(q=q, k=k, v=v, log_alpha=la, beta=b.contiguous(), S0=S0,
+                         cu_seqlens=cu, uniform=len(set(seq_lens)) <= 1, name=name)
+
+
+def workload_device(idx: int, device="cuda") -> PrefillInputs:
+    """Prefill workload ``idx`` (1..3) drawn on ``device``: same shapes, lengths,
+    distributions and specials as :func:`workload`, different values."""
+    if idx == 1:
+        return make_prefill_device([4096] * 4, 32, 128, seed=1, s0_std=0.02,
+                                   name=WORKLOADS[1], device=device)
+    if idx == 2:
+        return make_prefill_device([65536], 16, 128, seed=2, s0_std=0.0, log_alpha_fixed=-5.0,
+                                   log_alpha_fixed_channels=slice(0, 64), beta_mode="mix",
+                                   name=WORKLOADS[2], device=device)
+    if idx == 3:
+        return make_prefill_device(million_token_lengths(), 8, 128, seed=3, s0_std=0.02,
+                                   name=WORKLOADS[3], device=device)
+    raise ValueError(f"no device-drawn prefill workload {idx}")

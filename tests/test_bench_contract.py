@@ -39,3 +39,10 @@ def test_bench_line_has_the_contract_fields():
     cpu = rec["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] > 0
     assert rec["decode"]["roofline"]["frac"] > 0 and rec["decode_tokens"]["roofline"]["frac"] > 0
+    assert rec["clocks"]["samples"] >= 10  # the soak keeps the sampler under load
+    for leg in ("prefill_w2", "prefill_w3"):  # the long-context workloads, split across SMs
+        r = rec[leg]
+        assert r["value"] > 0 and "workload" in r
+        assert 0 < r["roofline"]["frac"] < 1.5 and r["roofline"]["bound"] == "hbm"
+        assert r["gpu_launches"] >= 3
+    assert rec["prefill_w3"]["cpu_baseline"]["kind"] == "oracle"
