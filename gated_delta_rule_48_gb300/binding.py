@@ -81,6 +81,30 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return _LIB
 
 
+class KdaTensor(ctypes.Structure):
+    """``kda_tensor`` of include/kda.h."""
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+KDA_DTYPE = {torch.bfloat16: 0, torch.float32: 1, torch.int32: 2}
+
+
+def describe(t):
+    """A kda_tensor for a torch tensor (None for None): pointer, dtype,
+    shape and strides exactly as torch holds them, unchecked."""
+    if t is None:
+        return None
+    d = KdaTensor()
+    d.data = t.data_ptr()
+    d.dtype = KDA_DTYPE.get(t.dtype, 99)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
 class _KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double)]
@@ -121,6 +145,13 @@ def load():
             lib.kda_last_error_message.restype = ctypes.c_char_p
             lib.kda_last_error_message.argtypes = []
             lib.kda_abi_version.restype = ctypes.c_int
+            tp = ctypes.POINTER(KdaTensor)
+            lib.kda_chunk_fwd_t.restype = ctypes.c_int
+            lib.kda_chunk_fwd_t.argtypes = [tp] * 9 + [vp]
+            lib.kda_decode_step_t.restype = ctypes.c_int
+            lib.kda_decode_step_t.argtypes = [tp] * 7 + [vp]
+            lib.kda_workspace_pool_bytes.restype = ctypes.c_int64
+            lib.kda_workspace_pool_bytes.argtypes = []
             lib.kda_selftest_bounded_wait.restype = ctypes.c_int
             lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
             lib.kda_profile_enable.restype = None
@@ -250,6 +281,33 @@ def kda_decode_step_fused(q_raw, k_raw, v, gate, beta, S_inout, out=None, *, str
                                         _ptr(beta), _ptr(S_inout), _ptr(out), N, H, dk, dv,
                                         _stream(stream)))
     return out
+
+
+def _dref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def kda_chunk_fwd_t(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, out=None, S_final=None,
+                    *, stream=None):
+    """The descriptor form of the prefill: tensors go to the library with their
+    dtype, shape and strides, and the library checks them.  ``out`` and
+    ``S_final`` must be given (None skips S_final)."""
+    descs = [describe(t) for t in (q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final)]
+    _check(load().kda_chunk_fwd_t(*[_dref(d) for d in descs], _stream(stream)))
+    return out, S_final
+
+
+def kda_decode_step_t(q, k, v, log_alpha, beta, S_inout, out, *, stream=None):
+    """The descriptor form of the decode step (see :func:`kda_chunk_fwd_t`)."""
+    descs = [describe(t) for t in (q, k, v, log_alpha, beta, S_inout, out)]
+    _check(load().kda_decode_step_t(*[_dref(d) for d in descs], _stream(stream)))
+    return out
+
+
+def kda_workspace_pool_bytes() -> int:
+    """Bytes reserved by the library's workspace pool on the current device,
+    or -1 when the library has created no pool there."""
+    return int(load().kda_workspace_pool_bytes())
 
 
 def kda_get_device_error(stream=None) -> int:

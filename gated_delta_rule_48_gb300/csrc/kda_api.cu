@@ -38,6 +38,10 @@ kda_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // ---------------------------------------------------------------- per device
+// The basic state (SM count, device address of the error word) is set up on
+// the first call of any entry point on a device.  The workspace pool is
+// created separately, on the first call that needs a workspace, so entry
+// points that allocate nothing never create or touch it.
 struct DeviceState {
   bool ready = false;
   int sm_count = 0;
@@ -48,7 +52,7 @@ struct DeviceState {
 std::mutex g_dev_mu;
 std::vector<DeviceState> g_devs;
 
-kda_status device_state(DeviceState** out) {
+kda_status device_state(DeviceState** out, bool want_pool = false) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -60,17 +64,24 @@ kda_status device_state(DeviceState** out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+    d.ready = true;
+  }
+  if (want_pool && !d.pool) {
     cudaMemPoolProps props;
     memset(&props, 0, sizeof props);
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
     props.location.id = dev;
-    e = cudaMemPoolCreate(&d.pool, &props);
+    cudaMemPool_t pool = nullptr;
+    e = cudaMemPoolCreate(&pool, &props);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
     uint64_t keep = ~0ull;  // keep freed workspace cached in the pool
-    e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
-    d.ready = true;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return cuda_fail(e, "cudaMemPoolSetAttribute");
+    }
+    d.pool = pool;
   }
   *out = &d;
   return KDA_OK;
@@ -163,17 +174,16 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
   return L;
 }
 
-// fused = false: q, k normalised by the caller, log_alpha f32.  fused = true:
-// q, k raw, and `log_alpha` points at the bf16 gate logits instead.
-static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
-                                 const void* log_alpha, const float* beta,
-                                 const float* S0, const int32_t* cu_seqlens, void* out,
-                                 float* S_final, int64_t T, int32_t N, int32_t H,
-                                 int32_t dk, int32_t dv, int64_t segment_tokens, bool fused,
-                                 int64_t ckpt_interval, float* ckpt, int64_t ckpt_max,
-                                 void* stream_v) {
+// Host-side checks of a prefill call; nothing is launched unless all pass.
+// Shared by every prefill entry point that takes device pointers, so they
+// reject the same arguments with the same status.
+kda_status check_prefill_args(const void* q, const void* k, const void* v,
+                              const void* log_alpha, const float* beta, const float* S0,
+                              const int32_t* cu_seqlens, const void* out, const float* S_final,
+                              int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv,
+                              int64_t segment_tokens, bool fused, int64_t ckpt_interval,
+                              const float* ckpt, int64_t ckpt_max) {
   const char* la_name = fused ? "gate" : "log_alpha";
-  // ---- host-side checks: nothing is launched unless all pass
   if (T < 0 || N < 0 || H <= 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "total_tokens=%lld n_seqs=%d n_heads=%d",
                 (long long)T, N, H);
@@ -231,7 +241,23 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
       return fail(KDA_ERR_INVALID_ARGUMENT, "S_final overlaps %s", r.name);
   }
   if (overlaps(r_out, r_sf)) return fail(KDA_ERR_INVALID_ARGUMENT, "out overlaps S_final");
-  if (N == 0) return KDA_OK;
+  return KDA_OK;
+}
+
+
+// fused = false: q, k normalised by the caller, log_alpha f32.  fused = true:
+// q, k raw, and `log_alpha` points at the bf16 gate logits instead.
+static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
+                                 const void* log_alpha, const float* beta,
+                                 const float* S0, const int32_t* cu_seqlens, void* out,
+                                 float* S_final, int64_t T, int32_t N, int32_t H,
+                                 int32_t dk, int32_t dv, int64_t segment_tokens, bool fused,
+                                 int64_t ckpt_interval, float* ckpt, int64_t ckpt_max,
+                                 void* stream_v) {
+  kda_status st = check_prefill_args(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, T,
+                                     N, H, dk, dv, segment_tokens, fused, ckpt_interval, ckpt,
+                                     ckpt_max);
+  if (st != KDA_OK || N == 0) return st;
 
   // ---- device work
   DeviceState* dev = nullptr;
@@ -267,6 +293,8 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   char* ws = nullptr;
   cudaError_t e = cudaSuccess;
   if (!direct) {
+    st = device_state(&dev, /*want_pool=*/true);
+    if (st != KDA_OK) return st;
     // Stream capture turns the allocation into a graph memory node, which takes
     // the default pool; otherwise the library's own pool keeps workspace cached.
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -326,6 +354,7 @@ extern "C" kda_status kda_chunk_fwd(const void* q, const void* k, const void* v,
                                     const float* S0, const int32_t* cu_seqlens, void* out,
                                     float* S_final, int64_t total_tokens, int32_t n_seqs,
                                     int32_t n_heads, int32_t dk, int32_t dv, void* stream) {
+  NvtxRange nvtx_range("kda_chunk_fwd");
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
                         n_seqs, n_heads, dk, dv, 0, false, 0, nullptr, 0, stream);
 }
@@ -335,6 +364,7 @@ extern "C" kda_status kda_chunk_fwd_fused(const void* q_raw, const void* k_raw, 
                                           const int32_t* cu_seqlens, void* out, float* S_final,
                                           int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
                                           int32_t dk, int32_t dv, void* stream) {
+  NvtxRange nvtx_range("kda_chunk_fwd_fused");
   return chunk_fwd_impl(q_raw, k_raw, v, gate, beta, S0, cu_seqlens, out, S_final, total_tokens,
                         n_seqs, n_heads, dk, dv, 0, true, 0, nullptr, 0, stream);
 }
@@ -345,6 +375,7 @@ extern "C" kda_status kda_chunk_fwd_split(const void* q, const void* k, const vo
                                           void* out, float* S_final, int64_t total_tokens,
                                           int32_t n_seqs, int32_t n_heads, int32_t dk,
                                           int32_t dv, int64_t segment_tokens, void* stream) {
+  NvtxRange nvtx_range("kda_chunk_fwd_split");
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
                         n_seqs, n_heads, dk, dv, segment_tokens, false, 0, nullptr, 0,
                         stream);
@@ -357,6 +388,7 @@ extern "C" kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, co
                                                 int32_t n_seqs, int32_t n_heads, int32_t dk,
                                                 int32_t dv, int64_t interval, float* checkpoints,
                                                 int64_t max_checkpoints, void* stream) {
+  NvtxRange nvtx_range("kda_chunk_fwd_checkpoints");
   if (interval <= 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint interval=%lld is not a positive multiple of %d",
                 (long long)interval, kChunk);
@@ -422,6 +454,7 @@ extern "C" kda_status kda_decode_step(const void* q, const void* k, const void* 
                                       const float* log_alpha, const float* beta,
                                       float* S_inout, void* out, int32_t N, int32_t H,
                                       int32_t dk, int32_t dv, void* stream) {
+  NvtxRange nvtx_range("kda_decode_step");
   return decode_impl(q, k, v, log_alpha, beta, S_inout, out, nullptr, N, 1, H, dk, dv, false,
                      stream);
 }
@@ -430,6 +463,7 @@ extern "C" kda_status kda_decode_step_fused(const void* q_raw, const void* k_raw
                                             const void* gate, const float* beta, float* S_inout,
                                             void* out, int32_t N, int32_t H, int32_t dk,
                                             int32_t dv, void* stream) {
+  NvtxRange nvtx_range("kda_decode_step_fused");
   return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, nullptr, N, 1, H, dk, dv, true,
                      stream);
 }
@@ -439,6 +473,7 @@ extern "C" kda_status kda_decode_tokens_fused(const void* q_raw, const void* k_r
                                               const float* beta, float* S_inout, void* out,
                                               const int32_t* commit, int32_t N, int32_t K,
                                               int32_t H, int32_t dk, int32_t dv, void* stream) {
+  NvtxRange nvtx_range("kda_decode_tokens_fused");
   return decode_impl(q_raw, k_raw, v, gate, beta, S_inout, out, commit, N, K, H, dk, dv, true,
                      stream);
 }
@@ -448,11 +483,13 @@ extern "C" kda_status kda_decode_tokens(const void* q, const void* k, const void
                                         float* S_inout, void* out, const int32_t* commit,
                                         int32_t N, int32_t K, int32_t H, int32_t dk, int32_t dv,
                                         void* stream) {
+  NvtxRange nvtx_range("kda_decode_tokens");
   return decode_impl(q, k, v, log_alpha, beta, S_inout, out, commit, N, K, H, dk, dv, false,
                      stream);
 }
 
 extern "C" kda_status kda_get_device_error(void* stream) {
+  NvtxRange nvtx_range("kda_get_device_error");
   DeviceState* dev = nullptr;
   kda_status st = device_state(&dev);
   if (st != KDA_OK) return st;
@@ -479,6 +516,7 @@ extern "C" kda_status kda_get_device_error(void* stream) {
 }
 
 extern "C" kda_status kda_selftest_bounded_wait(uint32_t polls, void* stream) {
+  NvtxRange nvtx_range("kda_selftest_bounded_wait");
   if (polls == 0 || polls > (1u << 20))
     return fail(KDA_ERR_INVALID_ARGUMENT, "polls must be in [1, 2^20] (got %u)", polls);
   DeviceState* dev = nullptr;
@@ -488,6 +526,21 @@ extern "C" kda_status kda_selftest_bounded_wait(uint32_t polls, void* stream) {
       launch_bounded_wait_selftest(polls, dev->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return KDA_OK;
+}
+
+extern "C" int64_t kda_workspace_pool_bytes(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev < (int)g_devs.size()) pool = g_devs[dev].pool;
+  }
+  if (!pool) return -1;
+  uint64_t reserved = 0;
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &reserved) != cudaSuccess)
+    return -1;
+  return static_cast<int64_t>(reserved);
 }
 
 extern "C" const char* kda_status_string(kda_status status) {

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "kda.h"
@@ -79,6 +80,26 @@ struct PrefillArgs {
 // ---- error reporting shared by the entry points (kda_api.cu)
 kda_status report_error(kda_status st, const char* msg);  // sets kda_last_error_message()
 kda_status device_error_word(int** out);                   // current device's error word
+// Host-side checks shared by the prefill entry points that take device
+// pointers (kda_api.cu); KDA_OK when the call may go ahead.
+kda_status check_prefill_args(const void* q, const void* k, const void* v,
+                              const void* log_alpha, const float* beta, const float* S0,
+                              const int32_t* cu_seqlens, const void* out, const float* S_final,
+                              int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv,
+                              int64_t segment_tokens, bool fused, int64_t ckpt_interval,
+                              const float* ckpt, int64_t ckpt_max);
+
+// ---- tracing: every C entry point opens an NVTX range named after itself
+// for its host-side duration (validation, planning, launches), so profilers
+// that record NVTX (Nsight Systems, ncu --nvtx) attribute the library's
+// kernels to the call that issued them.  Without such a tool attached the
+// push and pop are no-ops.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---- launch-time tracing (kda_api.cu)
 void prof_begin(cudaStream_t s, const char* name);

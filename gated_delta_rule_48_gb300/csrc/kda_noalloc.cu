@@ -59,14 +59,6 @@ kda_status scratch_address(unsigned char** out) {
   return KDA_OK;
 }
 
-bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
-
-bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
-  if (!a || !b || na <= 0 || nb <= 0) return false;
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-  return a0 < b0 + static_cast<uintptr_t>(nb) && b0 < a0 + static_cast<uintptr_t>(na);
-}
-
 }  // namespace
 
 }  // namespace kda
@@ -78,18 +70,12 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const 
                                             const float* S0, const int32_t* cu_seqlens,
                                             void* out, float* S_final, int64_t T, int32_t N,
                                             int32_t H, int32_t dk, int32_t dv, void* stream) {
-  // ---- host-side checks (same rules as kda_chunk_fwd), nothing launched on failure
-  if (T < 0 || N < 0 || H <= 0)
-    return report_error(KDA_ERR_INVALID_ARGUMENT, "total_tokens, n_seqs must be >= 0, n_heads > 0");
-  if (H > kMaxPrefillHeads)
-    return report_error(KDA_ERR_UNSUPPORTED, "n_heads exceeds 65535 (the prefill grid's second dimension)");
-  if (dk <= 0 || dv <= 0) return report_error(KDA_ERR_INVALID_ARGUMENT, "dk and dv must be positive");
-  if (dk != dv || (dk != 64 && dk != 128))
-    return report_error(KDA_ERR_UNSUPPORTED, "only dk == dv in {64, 128} is supported");
-  if (N == 0 && T > 0) return report_error(KDA_ERR_INVALID_ARGUMENT, "tokens given but n_seqs = 0");
-  if (!cu_seqlens && N > 0 && T % N != 0)
-    return report_error(KDA_ERR_INVALID_ARGUMENT,
-                        "cu_seqlens is NULL but total_tokens is not a multiple of n_seqs");
+  NvtxRange nvtx_range("kda_chunk_fwd_noalloc");
+  // ---- host-side checks: kda_chunk_fwd's own, plus the scratch limit;
+  // nothing is launched on failure
+  kda_status st = check_prefill_args(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, T, N,
+                                     H, dk, dv, 0, false, 0, nullptr, 0);
+  if (st != KDA_OK) return st;
   if (N > kNoAllocMaxSeqs) {
     char msg[160];
     snprintf(msg, sizeof msg,
@@ -98,30 +84,11 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const 
              N, kNoAllocMaxSeqs);
     return report_error(KDA_ERR_UNSUPPORTED, msg);
   }
-  if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !out))
-    return report_error(KDA_ERR_INVALID_ARGUMENT, "q, k, v, log_alpha, beta and out are required");
-  const void* all[] = {q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final};
-  for (const void* p : all)
-    if (misaligned16(p)) return report_error(KDA_ERR_INVALID_ARGUMENT, "a pointer is not 16-byte aligned");
-  const int64_t qk_b = T * H * dk * 2, v_b = T * H * dv * 2, la_b = T * H * dk * 4, b_b = T * H * 4;
-  const int64_t s_b = static_cast<int64_t>(N) * H * dk * dv * 4, cu_b = cu_seqlens ? (N + 1) * 4 : 0;
-  const struct { const void* p; int64_t n; } ins[] = {
-      {q, qk_b}, {k, qk_b}, {v, v_b}, {log_alpha, la_b}, {beta, b_b}, {S0, S0 ? s_b : 0},
-      {cu_seqlens, cu_b}};
-  for (int i = 0; i < 7; ++i) {
-    if (T > 0 && overlap(out, v_b, ins[i].p, ins[i].n))
-      return report_error(KDA_ERR_INVALID_ARGUMENT, "out overlaps an input");
-    const bool exact_alias = i == 5 && S_final == S0;
-    if (!exact_alias && overlap(S_final, S_final ? s_b : 0, ins[i].p, ins[i].n))
-      return report_error(KDA_ERR_INVALID_ARGUMENT, "S_final overlaps an input other than S0");
-  }
-  if (T > 0 && overlap(out, v_b, S_final, S_final ? s_b : 0))
-    return report_error(KDA_ERR_INVALID_ARGUMENT, "out overlaps S_final");
   if (N == 0) return KDA_OK;
 
   // ---- device work: planner + chunk kernels, plan kept in the fixed scratch
   unsigned char* scratch = nullptr;
-  kda_status st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != KDA_OK) return st;
   int* err = nullptr;
   st = device_error_word(&err);
