@@ -61,6 +61,7 @@ extern "C" kda_status kda_chunk_fwd_host(const void* q, const void* k, const voi
                                          int64_t total_tokens, int32_t n_seqs, int32_t H,
                                          int32_t dk, int32_t dv, int64_t slice_tokens,
                                          void* stream_v) {
+  NvtxRange nvtx_range("kda_chunk_fwd_host");
   const int64_t T = total_tokens;
   const int32_t N = n_seqs;
   if (T < 0 || N < 0 || H <= 0) return report_error(KDA_ERR_INVALID_ARGUMENT, "bad sizes");

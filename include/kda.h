@@ -114,6 +114,52 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          int32_t n_heads, int32_t dk, int32_t dv, void *stream);
 
 /*
+ * Tensor descriptors: kda_chunk_fwd_t, kda_decode_step_t.
+ *
+ * The same two layer calls with each tensor passed as a descriptor: device
+ * pointer, element type, rank, extents and strides (in elements).  The
+ * library then checks on the host, before anything is launched, what the
+ * pointer form must take on trust: every tensor's dtype (q, k, v, out bf16;
+ * log_alpha, beta, S0, S_final, S_inout f32; cu_seqlens i32), its rank, that
+ * its extents agree with q's (and v's for the value side), and that it is
+ * dense row-major (stride of the last dimension 1, each other stride the
+ * product of the extents after it; a dimension of extent 1 may have any
+ * stride).  A wrong dtype, a shape mismatch or a non-dense layout returns
+ * KDA_ERR_INVALID_ARGUMENT with kda_last_error_message() naming the tensor.
+ * Every other rule (alignment, overlaps, supported head sizes, ownership,
+ * streams, device-side errors) is the pointer form's; results are identical.
+ *
+ * kda_chunk_fwd_t: q is [T, H, dk] (packed; N = cu_seqlens' length - 1, or,
+ * without cu_seqlens, S0's or S_final's leading extent, else 1) or
+ * [B, T_b, H, dk] (a uniform batch of N = B sequences; cu_seqlens must then
+ * be NULL).  k, log_alpha have q's shape; v and out q's shape with dv last;
+ * beta q's shape without the last dimension; S0, S_final [N, H, dk, dv];
+ * cu_seqlens [N + 1].  S0, cu_seqlens and S_final may be NULL descriptors.
+ * kda_decode_step_t: q, k, log_alpha [N, H, dk]; v, out [N, H, dv]; beta
+ * [N, H]; S_inout [N, H, dk, dv].
+ * The descriptors are read during the call only.
+ */
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1, KDA_I32 = 2 } kda_dtype;
+
+typedef struct {
+    void *data;         /* device pointer to element [0, 0, ...] */
+    kda_dtype dtype;
+    int32_t ndim;       /* 1 .. 4 */
+    int64_t shape[4];   /* extents, outermost first */
+    int64_t stride[4];  /* in elements */
+} kda_tensor;
+
+kda_status kda_chunk_fwd_t(const kda_tensor *q, const kda_tensor *k,
+                           const kda_tensor *v, const kda_tensor *log_alpha,
+                           const kda_tensor *beta, const kda_tensor *S0,
+                           const kda_tensor *cu_seqlens, kda_tensor *out,
+                           kda_tensor *S_final, void *stream);
+kda_status kda_decode_step_t(const kda_tensor *q, const kda_tensor *k,
+                             const kda_tensor *v, const kda_tensor *log_alpha,
+                             const kda_tensor *beta, kda_tensor *S_inout,
+                             kda_tensor *out, void *stream);
+
+/*
  * kda_chunk_fwd_split -- kda_chunk_fwd with an explicit segment length.
  *
  * segment_tokens = 0 chooses automatically (what kda_chunk_fwd does).
@@ -147,13 +193,19 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
  * slower than kda_chunk_fwd.
  *
  * Limit: n_seqs <= 8184; larger batches return KDA_ERR_UNSUPPORTED (use
- * kda_chunk_fwd).  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the one array: calls that
- * overlap on the GPU (different streams, or different host threads without
- * ordering) race and may produce wrong results; order them on one stream.
- * Each call rebuilds the schedule it needs, so nothing carries over from
- * the previous call.
+ * kda_chunk_fwd).  Every other argument is checked exactly as kda_chunk_fwd
+ * checks it, with the same status codes.
+ *
+ * First call on a device: it sets up the library's per-device state -- the
+ * SM count and the device addresses of the error word and of the fixed array
+ * (cudaDeviceGetAttribute, cudaGetSymbolAddress), under a host mutex, with
+ * that device current -- and nothing else: it creates no memory pool (only
+ * the entry points that take a workspace do, on their own first use).  Make
+ * that first call before any stream capture.  All calls share the one array:
+ * calls that overlap on the GPU (different streams, or different host threads
+ * without ordering) race and may produce wrong results; order them on one
+ * stream.  Each call rebuilds the schedule it needs, so nothing carries over
+ * from the previous call.
  */
 kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  const float *log_alpha, const float *beta,
@@ -341,6 +393,15 @@ kda_status kda_decode_step_fused(const void *q_raw, const void *k_raw, const voi
  * KDA_ERR_CUDA when the synchronisation itself failed.
  */
 kda_status kda_get_device_error(void *stream);
+
+/*
+ * kda_workspace_pool_bytes -- memory accounting: the bytes the library's
+ * workspace pool currently reserves on the current device, or -1 when the
+ * library has created no pool there.  The pool is created by the first call
+ * that needs a workspace (kda_chunk_fwd on a packed batch, a split or
+ * checkpoints); it keeps freed workspace cached for the next call.
+ */
+int64_t kda_workspace_pool_bytes(void);
 
 /* Static description of a status code. */
 const char *kda_status_string(kda_status status);

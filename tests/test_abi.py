@@ -206,3 +206,70 @@ def test_selftest_rejects_bad_poll_counts(lib):
     # host-side checks only: nothing is launched
     assert lib.kda_selftest_bounded_wait(0, None) == 1  # KDA_ERR_INVALID_ARGUMENT
     assert lib.kda_selftest_bounded_wait((1 << 20) + 1, None) == 1
+
+
+NAMES9 = ["q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens", "out", "S_final"]
+
+# (description, overrides of prefill()'s arguments): each call is invalid or
+# unsupported for a reason found on the host
+BAD_PREFILL_CALLS = [
+    ("q misaligned", dict(q=P(0, 8))),
+    ("beta misaligned", dict(beta=P(4, 4))),
+    ("S_final misaligned", dict(S_final=P(8, 8))),
+    ("cu_seqlens misaligned", dict(cu_seqlens=P(6, 4))),
+    ("q missing", dict(q=None)),
+    ("out missing", dict(out=None)),
+    ("out inside q", dict(out=P(0, 64))),
+    ("S_final over v", dict(S_final=P(2))),
+    ("S_final partly over S0", dict(S_final=P(5, 16))),
+    ("out over S_final", dict(out=P(8, 16))),
+    ("dk != dv", dict(dk=128, dv=64)),
+    ("dk = 96", dict(dk=96, dv=96)),
+    ("dk = 0", dict(dk=0, dv=0)),
+    ("uniform batch that does not divide", dict(T=129, N=2)),
+    ("negative tokens", dict(T=-1)),
+    ("tokens without sequences", dict(T=10, N=0)),
+    ("no heads", dict(H=0)),
+    ("too many heads", dict(H=65536)),
+]
+
+
+@pytest.mark.parametrize("what,over", BAD_PREFILL_CALLS, ids=[c[0] for c in BAD_PREFILL_CALLS])
+def test_noalloc_rejects_what_kda_chunk_fwd_rejects(lib, what, over):
+    """The no-allocation entry point applies kda_chunk_fwd's host checks: the
+    same invalid call gets the same status (and a message) from both."""
+    dims = {k: over.pop(k) for k in ("T", "N", "H", "dk", "dv") if k in over}
+    full = dict(T=128, N=2, H=2, dk=64, dv=64)
+    full.update(dims)
+    p = {n: P(i) for i, n in enumerate(NAMES9)}
+    p["cu_seqlens"] = None
+    p.update(over)
+    args = [p[n] for n in NAMES9] + [full["T"], full["N"], full["H"], full["dk"], full["dv"]]
+    st_ref = lib.kda_chunk_fwd(*args, None)
+    msg_ref = lib.kda_last_error_message()
+    st = lib.kda_chunk_fwd_noalloc(*args, None)
+    msg = lib.kda_last_error_message()
+    assert st_ref in (INVALID, UNSUPPORTED), what
+    assert st == st_ref, (what, msg_ref, msg)
+    assert msg == msg_ref
+
+
+def test_no_file_names_a_line_of_the_source_pages():
+    """Sources are cited by page title and section, never by a line of the
+    extracted page file."""
+    bad = []
+    for dirpath, dirs, files in os.walk(ROOT):
+        dirs[:] = [d for d in dirs if not d.startswith((".", "_")) and d not in
+                   ("gpurun_out", "baseline", "__pycache__")]
+        for f in files:
+            if not f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".md", ".txt", ".json")):
+                continue
+            path = os.path.join(dirpath, f)
+            rel = os.path.relpath(path, ROOT)
+            if rel in ("SURVEY.md", "VERDICT.md", "ADVICE.md", "BASELINE.json") or \
+                    rel.startswith(("BENCH_", "GPUTEST_", "SCALE_", "MULTICHIP_")):
+                continue  # written by others, not by this project
+            with open(path, errors="replace") as fh:
+                if "PAPER" + ".md" in fh.read():
+                    bad.append(rel)
+    assert not bad, bad
