@@ -272,7 +272,9 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
         const float* kk = &s_kp[tt][quarter * RPT];
         const float* qq = &s_qp[tt][quarter * RPT];
         const float* ki = &s_ki[tt][quarter * RPT];
-        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;  // columns j (0) and j + 1 (1)
+        // a = (S'^T k)_{j, j+1}, b = (S'^T q)_{j, j+1}: packed two-lane
+        // multiply-adds (each lane rounds exactly as a scalar fmaf would)
+        float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < RPT; i += 4) {
           const float4 k4 = lds128_fresh(kk + i);
@@ -280,19 +282,17 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
           const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            a0 = fmaf(kv[x], st[i + x].x, a0);
-            a1 = fmaf(kv[x], st[i + x].y, a1);
-            b0 = fmaf(qv[x], st[i + x].x, b0);
-            b1 = fmaf(qv[x], st[i + x].y, b1);
+            a = __ffma2_rn(make_float2(kv[x], kv[x]), st[i + x], a);
+            b = __ffma2_rn(make_float2(qv[x], qv[x]), st[i + x], b);
           }
         }
         // sum over the four quarters, in quarter order (every thread of a
         // column pair gets the same sums)
         const int par = 2 * (t & 1);
-        *reinterpret_cast<float2*>(&s_part[par][quarter][j]) = make_float2(a0, a1);
-        *reinterpret_cast<float2*>(&s_part[par + 1][quarter][j]) = make_float2(b0, b1);
+        *reinterpret_cast<float2*>(&s_part[par][quarter][j]) = a;
+        *reinterpret_cast<float2*>(&s_part[par + 1][quarter][j]) = b;
         __syncthreads();
-        a0 = a1 = b0 = b1 = 0.f;
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const float2 pa = *reinterpret_cast<const float2*>(&s_part[par][x][j]);
@@ -304,15 +304,13 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
           *reinterpret_cast<uint32_t*>(out + row * D + j) =
               static_cast<uint32_t>(f32_to_bf16(b0 + s_qk[tt] * u0)) |
               (static_cast<uint32_t>(f32_to_bf16(b1 + s_qk[tt] * u1)) << 16);
+        const float2 u = make_float2(u0, u1);
 #pragma unroll
         for (int i = 0; i < RPT; i += 4) {
           const float4 k4 = lds128_fresh(ki + i);
           const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            st[i + x].x = fmaf(kv[x], u0, st[i + x].x);
-            st[i + x].y = fmaf(kv[x], u1, st[i + x].y);
-          }
+          for (int x = 0; x < 4; ++x) st[i + x] = __ffma2_rn(make_float2(kv[x], kv[x]), u, st[i + x]);
         }
         if (t + 1 == n_commit) {  // S = P Z
           const float* pp = &s_P[tt][quarter * RPT];
@@ -323,7 +321,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
 #pragma unroll
             for (int x = 0; x < 4; ++x)
               __stcs(reinterpret_cast<float2*>(Sc + static_cast<int64_t>(i + x) * D),
-                     make_float2(st[i + x].x * pv[x], st[i + x].y * pv[x]));
+                     __fmul2_rn(st[i + x], make_float2(pv[x], pv[x])));
           }
         }
       }
@@ -334,10 +332,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
           const float4 p4 = lds128_fresh(pp + i);
           const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            st[i + x].x *= pv[x];
-            st[i + x].y *= pv[x];
-          }
+          for (int x = 0; x < 4; ++x) st[i + x] = __fmul2_rn(st[i + x], make_float2(pv[x], pv[x]));
         }
       }
       __syncthreads();  // the next batch (or unit) rewrites the token vectors

@@ -130,6 +130,31 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // Barrier among the 16 worker warps only (the control warps never join it).
 __device__ __forceinline__ void worker_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
+// Packed two-lane fp32 arithmetic (each lane rounds exactly as the scalar
+// operation would): half the instructions of the scalar form.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 bcast2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  return __fadd2_rn(a, make_float2(-b.x, -b.y));
+}
+// 4 bf16 (two 32-bit words) -> channels 0, 1 and 2, 3 as float2 pairs
+__device__ __forceinline__ void unpack4x2(uint2 u, float2& f01, float2& f23) {
+  f01 = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+  f23 = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ uint2 pack4x2_bf16(float2 f01, float2 f23) {
+  return make_uint2(pack_bf16x2(f01.x, f01.y), pack_bf16x2(f23.x, f23.y));
+}
+__device__ __forceinline__ uint4 pack4x2_tf32(float2 f01, float2 f23) {
+  return make_uint4(f32_to_tf32_rn(f01.x), f32_to_tf32_rn(f01.y), f32_to_tf32_rn(f23.x),
+                    f32_to_tf32_rn(f23.y));
+}
+__device__ __forceinline__ float2 rcp2(float2 a) { return make_float2(rcp_approx(a.x), rcp_approx(a.y)); }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
 __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
   f[0] = __uint_as_float(u.x << 16);
   f[1] = __uint_as_float(u.x & 0xffff0000u);
@@ -268,9 +293,9 @@ __device__ void ut_front(float* __restrict__ sA, float* __restrict__ Xs,
       const int a = 2 * h + 1, b = 2 * h;
       const int r = lane >> 1, c0 = 8 * (lane & 1);
       float* X = Xs + h * 256;  // [16][16]
-      float acc[8];
+      float2 acc[4];  // columns c0 + (0, 1), (2, 3), (4, 5), (6, 7)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
       const float* Arow = sA + (16 * a + r) * kLdA + 16 * b;
       const float* Db = sA + (16 * b) * kLdA + 16 * b + c0;
 #pragma unroll
@@ -280,19 +305,17 @@ __device__ void ut_front(float* __restrict__ sA, float* __restrict__ Xs,
         for (int u = 0; u < 4; ++u) {
           const float4 d0 = *reinterpret_cast<const float4*>(Db + (i4 + u) * kLdA);
           const float4 d1 = *reinterpret_cast<const float4*>(Db + (i4 + u) * kLdA + 4);
-          const float s = f4c(av, u);
-          acc[0] = fmaf(s, d0.x, acc[0]); acc[1] = fmaf(s, d0.y, acc[1]);
-          acc[2] = fmaf(s, d0.z, acc[2]); acc[3] = fmaf(s, d0.w, acc[3]);
-          acc[4] = fmaf(s, d1.x, acc[4]); acc[5] = fmaf(s, d1.y, acc[5]);
-          acc[6] = fmaf(s, d1.z, acc[6]); acc[7] = fmaf(s, d1.w, acc[7]);
+          const float2 s = bcast2(f4c(av, u));
+          acc[0] = fma2(s, lo2(d0), acc[0]); acc[1] = fma2(s, hi2(d0), acc[1]);
+          acc[2] = fma2(s, lo2(d1), acc[2]); acc[3] = fma2(s, hi2(d1), acc[3]);
         }
       }
-      *reinterpret_cast<float4*>(X + r * 16 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(X + r * 16 + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      *reinterpret_cast<float4*>(X + r * 16 + c0) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+      *reinterpret_cast<float4*>(X + r * 16 + c0 + 4) = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
       __syncwarp();
       const float* Da = sA + (16 * a + r) * kLdA + 16 * a;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i4 = 0; i4 < 16; i4 += 4) {
         const float4 dv = *reinterpret_cast<const float4*>(Da + i4);
@@ -300,16 +323,14 @@ __device__ void ut_front(float* __restrict__ sA, float* __restrict__ Xs,
         for (int u = 0; u < 4; ++u) {
           const float4 x0 = *reinterpret_cast<const float4*>(X + (i4 + u) * 16 + c0);
           const float4 x1 = *reinterpret_cast<const float4*>(X + (i4 + u) * 16 + c0 + 4);
-          const float s = f4c(dv, u);
-          acc[0] = fmaf(s, x0.x, acc[0]); acc[1] = fmaf(s, x0.y, acc[1]);
-          acc[2] = fmaf(s, x0.z, acc[2]); acc[3] = fmaf(s, x0.w, acc[3]);
-          acc[4] = fmaf(s, x1.x, acc[4]); acc[5] = fmaf(s, x1.y, acc[5]);
-          acc[6] = fmaf(s, x1.z, acc[6]); acc[7] = fmaf(s, x1.w, acc[7]);
+          const float2 s = bcast2(f4c(dv, u));
+          acc[0] = fma2(s, lo2(x0), acc[0]); acc[1] = fma2(s, hi2(x0), acc[1]);
+          acc[2] = fma2(s, lo2(x1), acc[2]); acc[3] = fma2(s, hi2(x1), acc[3]);
         }
       }
       float* Tab = sA + (16 * a + r) * kLdA + 16 * b + c0;  // A_ab was read before the last sync
-      *reinterpret_cast<float4*>(Tab) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-      *reinterpret_cast<float4*>(Tab + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+      *reinterpret_cast<float4*>(Tab) = make_float4(-acc[0].x, -acc[0].y, -acc[1].x, -acc[1].y);
+      *reinterpret_cast<float4*>(Tab + 4) = make_float4(-acc[2].x, -acc[2].y, -acc[3].x, -acc[3].y);
     }
   } else {
     // T'_(01) = 0: rows 0..31, columns 32..63 of the tf32 copy (256 chunks of
@@ -336,7 +357,7 @@ __device__ void ut_back(float* __restrict__ sA, float* __restrict__ Xs,
     // (warps w, w + 4) gets the same number of steps
     const int q = warp < 4 ? warp : 11 - warp;
     const int r = lane;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 x01 = make_float2(0.f, 0.f), x23 = make_float2(0.f, 0.f);
     for (int i0 = 4 * q; i0 < 32; i0 += 4) {  // T'_(00)[i][4q..] = 0 for i < 4q
       float av[4];
       float4 t[4];
@@ -347,32 +368,28 @@ __device__ void ut_back(float* __restrict__ sA, float* __restrict__ Xs,
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        x[0] = fmaf(av[u], t[u].x, x[0]);
-        x[1] = fmaf(av[u], t[u].y, x[1]);
-        x[2] = fmaf(av[u], t[u].z, x[2]);
-        x[3] = fmaf(av[u], t[u].w, x[3]);
+        x01 = fma2(bcast2(av[u]), lo2(t[u]), x01);
+        x23 = fma2(bcast2(av[u]), hi2(t[u]), x23);
       }
     }
-    *reinterpret_cast<float4*>(Xs + r * 36 + 4 * q) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(Xs + r * 36 + 4 * q) = make_float4(x01.x, x01.y, x23.x, x23.y);
     __syncwarp();
     // T'_(11) is stored in full (zeros above its diagonal): 32 terms per row
     const float* T11 = sA + (32 + r) * kLdA + 32;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int i0 = 0; i0 < 32; i0 += 4) {
       const float4 tv = *reinterpret_cast<const float4*>(T11 + i0);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float4 xv = *reinterpret_cast<const float4*>(Xs + (i0 + u) * 36 + 4 * q);
-        const float s = f4c(tv, u);
-        y[0] = fmaf(s, xv.x, y[0]);
-        y[1] = fmaf(s, xv.y, y[1]);
-        y[2] = fmaf(s, xv.z, y[2]);
-        y[3] = fmaf(s, xv.w, y[3]);
+        const float2 s = bcast2(f4c(tv, u));
+        y01 = fma2(s, lo2(xv), y01);
+        y23 = fma2(s, hi2(xv), y23);
       }
     }
     const float4 bq = *reinterpret_cast<const float4*>(sBeta + 4 * q);
-    put_T4(R, 32 + r, q, make_float4(-y[0] * bq.x, -y[1] * bq.y, -y[2] * bq.z, -y[3] * bq.w));
+    put_T4(R, 32 + r, q, make_float4(-y01.x * bq.x, -y01.y * bq.y, -y23.x * bq.z, -y23.y * bq.w));
   } else {
     // T'_(00) and T'_(11) to T: 2 halves x 32 rows x 8 column groups
     for (int e = tid - 256; e < 512; e += 256) {
@@ -387,7 +404,7 @@ __device__ void ut_back(float* __restrict__ sA, float* __restrict__ Xs,
 // Per-thread values of one chunk kept between steps: this thread's tokens
 // 4w .. 4w+3 (w = warp) and channels 4l .. 4l+3 (l = lane).
 struct ChunkRegs {
-  float e[4][4];    // e^{g - G} (G = the strip's anchor)
+  float2 e[4][2];   // e^{g - G} (G = the strip's anchor): channels (0, 1), (2, 3)
   uint2 kraw[4];    // k (4 bf16)
   uint2 qraw[4];    // q (4 bf16)
 };
@@ -415,8 +432,10 @@ template <int MODE, bool FUSED, bool CKPT>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived from the shared array by an offset so the
+  // compiler keeps every access in the shared window (32-bit addressing,
+  // ld.shared / st.shared) instead of falling back to generic accesses
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t seg_id = blockIdx.x;
   const int h = blockIdx.y;
@@ -537,8 +556,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     *s_abort = 1;
   };
   // worker side: wait for MMA group g of chunk n; signal that group g's operands are ready
-  auto wait_done = [&](int g, int64_t n) {
-    if (!mbar_wait(bar_done + g, static_cast<uint32_t>(n & 1))) flag_timeout();
+  // MMA group g of chunk n has completed: warp 0 alone polls its mbarrier,
+  // the worker barrier then releases the other 15 warps (who would otherwise
+  // each poll, taking issue slots from the warps still working)
+  auto wait_done_sync = [&](int g, int64_t n) {
+    if (warp == 0 && !mbar_wait(bar_done + g, static_cast<uint32_t>(n & 1))) flag_timeout();
+    worker_sync();
     tc_fence_after();
   };
   auto signal_ready = [&](int g) {
@@ -594,31 +617,32 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   auto scan_chunk = [&](int64_t m) {
     const int valid = chunk_valid(m);
     if (!mbar_wait(bar_qkl, static_cast<uint32_t>(m & 1))) flag_timeout();
-    float g[4][4];
+    float2 g[4][2];
     {
-      float run[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 run01 = make_float2(0.f, 0.f), run23 = make_float2(0.f, 0.f);
+      const bool full = valid == C;  // warp-uniform: no token of the chunk is past the end
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = r0 + i;
-        const bool ok = r < valid;
-        float la[4];
+        const bool ok = full || r < valid;
+        float2 la01, la23;
         if (FUSED) {  // gate logits, bf16
           float gf[4];
           unpack4(*reinterpret_cast<const uint2*>(sm + kRawL + sw128_offset(C, r, 8 * lane)), gf);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) la[x] = gate_log_alpha_fast(gf[x]);
+          la01 = make_float2(gate_log_alpha_fast(gf[0]), gate_log_alpha_fast(gf[1]));
+          la23 = make_float2(gate_log_alpha_fast(gf[2]), gate_log_alpha_fast(gf[3]));
         } else {
           const float4 l4 =
               *reinterpret_cast<const float4*>(sm + kRawL + sw128_offset(C, r, 16 * lane));
-          la[0] = clamp_log_alpha(l4.x); la[1] = clamp_log_alpha(l4.y);
-          la[2] = clamp_log_alpha(l4.z); la[3] = clamp_log_alpha(l4.w);
+          la01 = make_float2(clamp_log_alpha(l4.x), clamp_log_alpha(l4.y));
+          la23 = make_float2(clamp_log_alpha(l4.z), clamp_log_alpha(l4.w));
         }
-        run[0] += ok ? la[0] : 0.f;
-        run[1] += ok ? la[1] : 0.f;
-        run[2] += ok ? la[2] : 0.f;
-        run[3] += ok ? la[3] : 0.f;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) g[i][x] = run[x];
+        if (ok) {
+          run01 = add2(run01, la01);
+          run23 = add2(run23, la23);
+        }
+        g[i][0] = run01;
+        g[i][1] = run23;
         cr.kraw[i] = ok ? *reinterpret_cast<const uint2*>(sm + kRawK + sw128_offset(C, r, 8 * lane))
                         : make_uint2(0u, 0u);
         cr.qraw[i] = (kOut && ok)
@@ -629,7 +653,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_raw);  // this warp is done with the raw tiles
       *reinterpret_cast<float4*>(sTot + warp * 128 + 4 * lane) =
-          make_float4(run[0], run[1], run[2], run[3]);
+          make_float4(run01.x, run01.y, run23.x, run23.y);
     }
     if (tid < C) sBeta[tid] = beta_reg;
     worker_sync();
@@ -663,19 +687,16 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
     worker_sync();
     {
+      // g - G = (within-warp prefix) + (exclusive prefix of the earlier warps - G)
       const float4 off = *reinterpret_cast<const float4*>(sTot + warp * 128 + 4 * lane);
+      const float4 gA = *reinterpret_cast<const float4*>((strip ? sG1 : sG0) + 4 * lane);
+      const float2 d01 = sub2(lo2(off), lo2(gA)), d23 = sub2(hi2(off), hi2(gA));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        g[i][0] += off.x; g[i][1] += off.y; g[i][2] += off.z; g[i][3] += off.w;
+        const float2 x01 = add2(g[i][0], d01), x23 = add2(g[i][1], d23);
+        cr.e[i][0] = make_float2(__expf(x01.x), __expf(x01.y));  // in [e^-80, e^80]
+        cr.e[i][1] = make_float2(__expf(x23.x), __expf(x23.y));
       }
-    }
-    {
-      const float4 gA = *reinterpret_cast<const float4*>((strip ? sG1 : sG0) + 4 * lane);
-      const float G[4] = {gA.x, gA.y, gA.z, gA.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) cr.e[i][x] = __expf(g[i][x] - G[x]);  // in [e^-80, e^80]
     }
   };
 
@@ -689,36 +710,31 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     unsigned char* Bop = R + 32768;   // bf16 [96][128]: keys 0..31 (strip-0 anchor) | keys 0..63
     const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
     const float4 e104 = *reinterpret_cast<const float4*>(sPC + 4 * 128 + 4 * lane);
-    const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w}, e10[4] = {e104.x, e104.y, e104.z, e104.w};
-    float kgT[4][4];                  // [channel x][token i] of k e^g
+    const float2 eG01 = lo2(eg4), eG23 = hi2(eg4), e1001 = lo2(e104), e1023 = hi2(e104);
+    float kgT[4][4];                  // [channel x][token i] of k e^g (summary)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = r0 + i, rr = r & 31;
-      float kf[4], qf[4], qt[4], kt[4], kh[4];
-      unpack4(cr.kraw[i], kf);
-      unpack4(cr.qraw[i], qf);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float inv = rcp_approx(cr.e[i][x]);
-        qt[x] = qf[x] * cr.e[i][x];
-        kt[x] = kf[x] * cr.e[i][x];
-        kh[x] = kf[x] * inv;
-        kgT[x][i] = kt[x] * eG[x];
-      }
-      if (kP) *reinterpret_cast<uint4*>(KG + sw128_offset(C, r, 16 * lane)) =
-          make_uint4(f32_to_tf32_rn(kgT[0][i]), f32_to_tf32_rn(kgT[1][i]),
-                     f32_to_tf32_rn(kgT[2][i]), f32_to_tf32_rn(kgT[3][i]));
-      *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + rr, 8 * lane)) = pack4_bf16(qt);
+      float2 kf01, kf23, qf01, qf23;
+      unpack4x2(cr.kraw[i], kf01, kf23);
+      unpack4x2(cr.qraw[i], qf01, qf23);
+      const float2 e01 = cr.e[i][0], e23 = cr.e[i][1];
+      const float2 qt01 = mul2(qf01, e01), qt23 = mul2(qf23, e23);
+      const float2 kt01 = mul2(kf01, e01), kt23 = mul2(kf23, e23);
+      const float2 kh01 = mul2(kf01, rcp2(e01)), kh23 = mul2(kf23, rcp2(e23));
+      const float2 kg01 = mul2(kt01, eG01), kg23 = mul2(kt23, eG23);
+      kgT[0][i] = kg01.x; kgT[1][i] = kg01.y; kgT[2][i] = kg23.x; kgT[3][i] = kg23.y;
+      if (kP) *reinterpret_cast<uint4*>(KG + sw128_offset(C, r, 16 * lane)) = pack4x2_tf32(kg01, kg23);
+      *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + rr, 8 * lane)) =
+          pack4x2_bf16(qt01, qt23);
       *reinterpret_cast<uint2*>(Aop + sw128_offset(128, 64 * strip + 32 + rr, 8 * lane)) =
-          pack4_bf16(kt);
+          pack4x2_bf16(kt01, kt23);
       if (strip == 0) {
-        float kh1[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) kh1[x] = kh[x] * e10[x];
-        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, r, 8 * lane)) = pack4_bf16(kh);
-        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh1);
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, r, 8 * lane)) = pack4x2_bf16(kh01, kh23);
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) =
+            pack4x2_bf16(mul2(kh01, e1001), mul2(kh23, e1023));
       } else {
-        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4_bf16(kh);
+        *reinterpret_cast<uint2*>(Bop + sw128_offset(96, 32 + r, 8 * lane)) = pack4x2_bf16(kh01, kh23);
       }
     }
     if (!kP) {
@@ -791,26 +807,35 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   // tf32 into KG (the B operand of O^T = S^T (q e^g)^T)
   auto write_qeg = [&]() {
     const float4 eg4 = *reinterpret_cast<const float4*>(sPC + (strip ? 1 : 0) * 128 + 4 * lane);
-    const float eG[4] = {eg4.x, eg4.y, eg4.z, eg4.w};
+    const float2 eG01 = lo2(eg4), eG23 = hi2(eg4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float qf[4], f[4];
-      unpack4(cr.qraw[i], qf);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) f[x] = qf[x] * cr.e[i][x] * eG[x];
-      *reinterpret_cast<uint4*>(KG + sw128_offset(C, r0 + i, 16 * lane)) = pack4_tf32(f);
+      float2 qf01, qf23;
+      unpack4x2(cr.qraw[i], qf01, qf23);
+      const float2 f01 = mul2(mul2(qf01, cr.e[i][0]), eG01), f23 = mul2(mul2(qf23, cr.e[i][1]), eG23);
+      *reinterpret_cast<uint4*>(KG + sw128_offset(C, r0 + i, 16 * lane)) = pack4x2_tf32(f01, f23);
     }
   };
   auto decay_round = [&](uint32_t cs, uint32_t cu, int64_t n) {
+    const float* gl = sEGl + (n & 1) * 128 + 32 * part;
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
       const uint32_t ta = tmem_addr(tmem, 32 * quad, cs + 32 * part + cc);
       uint32_t sv[16];
       tmem_ld16(ta, sv);
+      float4 gv[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) gv[y] = *reinterpret_cast<const float4*>(gl + cc + 4 * y);
       tmem_wait_ld();
 #pragma unroll
-      for (int x = 0; x < 16; ++x)
-        sv[x] = __float_as_uint(__uint_as_float(sv[x]) * sEGl[(n & 1) * 128 + 32 * part + cc + x]);
+      for (int y = 0; y < 4; ++y) {
+        const float2 a = mul2(make_float2(__uint_as_float(sv[4 * y]), __uint_as_float(sv[4 * y + 1])),
+                              lo2(gv[y]));
+        const float2 b = mul2(make_float2(__uint_as_float(sv[4 * y + 2]), __uint_as_float(sv[4 * y + 3])),
+                              hi2(gv[y]));
+        sv[4 * y] = __float_as_uint(a.x); sv[4 * y + 1] = __float_as_uint(a.y);
+        sv[4 * y + 2] = __float_as_uint(b.x); sv[4 * y + 3] = __float_as_uint(b.y);
+      }
       tmem_st16(ta, sv);
     }
     const uint32_t tu = tmem_addr(tmem, 32 * quad, cu + 16 * part);
@@ -1040,8 +1065,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 
       // ---- A: strip products (bf16) -> TMEM  ||  out of chunk n-1
       if (kOut && n > 0) write_out(n - 1);
-      wait_done(0, n);
-      worker_sync();
+      wait_done_sync(0, n);
       if (*s_abort) break;
 
       // ---- B: strip read-out, UT transform, T to SMEM
@@ -1100,7 +1124,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       // which are free here) and q e^g into KG (P^T's B operand is consumed);
       // warps 0 and 1 write their q e^g after the transform
       if (kP && warp >= 2) {
-        if (!mbar_wait(bar_donep, static_cast<uint32_t>(n & 1))) flag_timeout();
+        if (warp == 2 && !mbar_wait(bar_donep, static_cast<uint32_t>(n & 1))) flag_timeout();
+        asm volatile("bar.sync 3, 448;" ::: "memory");  // warps 2..15
         tc_fence_after();
         round_neg_p();
         write_qeg();
@@ -1120,14 +1145,15 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       {
         // K' = k e^{g_last - g} = k e^{G - g} e^{g_last - G}, transposed [c][t]
         const float4 gl4 = *reinterpret_cast<const float4*>(sPC + (strip ? 3 : 2) * 128 + 4 * lane);
-        const float eglG[4] = {gl4.x, gl4.y, gl4.z, gl4.w};
+        const float2 gl01 = lo2(gl4), gl23 = hi2(gl4);
         float kp[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float kf[4];
-          unpack4(cr.kraw[i], kf);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) kp[x][i] = kf[x] * rcp_approx(cr.e[i][x]) * eglG[x];
+          float2 kf01, kf23;
+          unpack4x2(cr.kraw[i], kf01, kf23);
+          const float2 p01 = mul2(mul2(kf01, rcp2(cr.e[i][0])), gl01);
+          const float2 p23 = mul2(mul2(kf23, rcp2(cr.e[i][1])), gl23);
+          kp[0][i] = p01.x; kp[1][i] = p01.y; kp[2][i] = p23.x; kp[3][i] = p23.y;
         }
         uint4 kv[4];
 #pragma unroll
@@ -1135,8 +1161,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         st_transposed4(KP, lane, r0, kv);
       }
       if (kP && n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
-      wait_done(1, n);
-      worker_sync();
+      wait_done_sync(1, n);
       if (*s_abort) break;
 
       if (!kP) {  // summary: phases D and E
@@ -1156,8 +1181,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 
       // ---- E: U^T -= S^T W^T (A = S^T in TMEM)  ||  scan of chunk n+1
       if (n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
-      wait_done(2, n);
-      worker_sync();
+      wait_done_sync(2, n);
       if (*s_abort) break;
       }
 
@@ -1172,8 +1196,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         build_chunk();  // chunk n+1 operands into freed buffers
         signal_ready(0);
       }
-      wait_done(3, n);
-      worker_sync();
+      wait_done_sync(3, n);
       if (CKPT) {  // the state after this chunk, if the sequence has a checkpoint here
         // tokens of the sequence up to this chunk's end (< 2^31: TMA coordinates are 32-bit)
         const int32_t ci = static_cast<int32_t>(a.plan.ckpt_interval);

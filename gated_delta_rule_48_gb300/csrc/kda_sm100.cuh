@@ -47,12 +47,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls (each poll itself blocks for a
-// hardware-chosen interval) and returns false instead of spinning forever.
+// One poll that may suspend the thread until the phase completes or about
+// `hint_ns` nanoseconds pass (the suspend-time hint of try_wait), whichever
+// comes first: a waiting warp then issues a few instructions per hint instead
+// of one poll every few cycles, leaving the issue slots to working warps.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls (each suspends the thread for at
+// most about 2 microseconds, and returns as soon as the phase completes) and
+// returns false instead of spinning forever: at most about 2 s by default.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint32_t limit = 1u << 22) {
+                                          uint32_t limit = 1u << 20) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
   return false;
 }
 
