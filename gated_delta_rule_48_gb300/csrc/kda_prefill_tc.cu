@@ -32,7 +32,9 @@
 // Operand precision: strip products in bf16 (their error only perturbs T and
 // the output); T is fp32 and enters the tf32 MMA rounded to nearest, and the
 // bf16 MMA with V (exact in bf16) as a hi + lo pair of bf16; every operand on
-// the state path is tf32 rounded to nearest; accumulation is fp32.  tf32
+// the state path is tf32 rounded to nearest; the two output-only operands
+// (q e^g and A_qk) are stored fp32 and read by the tensor core as tf32, i.e.
+// truncated; accumulation is fp32.  tf32
 // operands are always laid out K-major: K' (and, for W^T, k e^g) are written
 // transposed, [key channel][token]; k e^g for P^T and q e^g [token][channel].
 //
@@ -160,9 +162,6 @@ __device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
   f[1] = __uint_as_float(u.x & 0xffff0000u);
   f[2] = __uint_as_float(u.y << 16);
   f[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-__device__ __forceinline__ uint2 pack4_bf16(const float (&f)[4]) {
-  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
 }
 // Fused input preparation.  The 8 vectors k_r, q_r of a warp's 4 tokens each
 // span the warp (4 channels per lane); each is scaled to unit L2 norm,
@@ -813,7 +812,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       float2 qf01, qf23;
       unpack4x2(cr.qraw[i], qf01, qf23);
       const float2 f01 = mul2(mul2(qf01, cr.e[i][0]), eG01), f23 = mul2(mul2(qf23, cr.e[i][1]), eG23);
-      *reinterpret_cast<uint4*>(KG + sw128_offset(C, r0 + i, 16 * lane)) = pack4x2_tf32(f01, f23);
+      // fp32 as is: the tensor core reads it as tf32 by truncation, which on
+      // this output-only operand costs well under the rounding budget
+      *reinterpret_cast<float4*>(KG + sw128_offset(C, r0 + i, 16 * lane)) =
+          make_float4(f01.x, f01.y, f23.x, f23.y);
     }
   };
   auto decay_round = [&](uint32_t cs, uint32_t cu, int64_t n) {
@@ -1101,7 +1103,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
             }
           }
           else if (kOut)
-            *reinterpret_cast<uint4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) = pack4_tf32(f);
+            *reinterpret_cast<float4*>(R + kRAqk + sw128_offset(C, r, 4 * i)) =
+                make_float4(f[0], f[1], f[2], f[3]);  // output-only: read truncated
         }
         if (s == 0) {  // strip-0 rows have no keys >= 32
           const int iz = 32 + 8 * part;
