@@ -314,8 +314,11 @@ def long_leg(kb, idx, steps, warmup, world, peaks, peak_src):
     top_name, (top_n, top_ms) = max(kernels.items(), key=lambda kv: kv[1][1])
     tflops = alg_flops / (ms * 1e-3) / 1e12
     attainable = min(peaks["bf16_tflops"], alg_flops / alg_bytes * peaks["hbm_gbs"] / 1e3)
+    # DRAM bytes per step from the committed ncu records of each kernel; the
+    # planner reads at most cu_seqlens and writes the segment list (a few KB),
+    # so it counts as zero
     traffic = None
-    recs = [recorded_traffic_leg(name, idx) for name in kernels]
+    recs = [0.0 if name == "kda_plan" else recorded_traffic_leg(name, idx) for name in kernels]
     if kernels and all(r is not None for r in recs):
         traffic = sum(r * (n / steps) for r, (n, _) in zip(recs, kernels.values()))
     leg = {
@@ -670,9 +673,17 @@ def main():
     launches = sum(n for n, _ in kernels.values())
     top_name, (top_n, top_ms) = max(kernels.items(), key=lambda kv: kv[1][1])
     top_avg_ms = top_ms / top_n
-    # algorithmic bytes per launch: the replay launch covers the whole batch once
-    per_launch_bytes = alg_bytes * (args.steps / top_n)
-    achieved_gbs = per_launch_bytes / (top_avg_ms * 1e-3) / 1e9
+    if len(kernels) == 1:
+        # one kernel per step (the batched workload): its launch covers the
+        # whole batch once, so the step's algorithmic bytes are its own
+        per_launch_bytes = alg_bytes * (args.steps / top_n)
+        achieved_gbs = per_launch_bytes / (top_avg_ms * 1e-3) / 1e9
+    else:
+        # several kernels per step (a split workload): the roofline of the
+        # whole path, the step's bytes over the summed kernel time per step
+        per_launch_bytes = alg_bytes
+        achieved_gbs = alg_bytes / (sum(t for _, t in kernels.values()) / args.steps * 1e-3) / 1e9
+        top_name = "whole path: " + ", ".join(sorted(kernels))
     tflops = alg_flops / (ms * 1e-3) / 1e12
     traffic = recorded_traffic(top_name, "kda_prefill_tc.cu")
 
