@@ -11,6 +11,7 @@ import os
 import subprocess
 import threading
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -150,6 +151,9 @@ def load():
             lib.kda_chunk_fwd_t.argtypes = [tp] * 9 + [vp]
             lib.kda_decode_step_t.restype = ctypes.c_int
             lib.kda_decode_step_t.argtypes = [tp] * 7 + [vp]
+            lib.kda_debug_chunk_dump.restype = ctypes.c_int
+            lib.kda_debug_chunk_dump.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, i32, i32, i64,
+                                                         vp, vp]
             lib.kda_workspace_pool_bytes.restype = ctypes.c_int64
             lib.kda_workspace_pool_bytes.argtypes = []
             lib.kda_selftest_bounded_wait.restype = ctypes.c_int
@@ -302,6 +306,39 @@ def kda_decode_step_t(q, k, v, log_alpha, beta, S_inout, out, *, stream=None):
     descs = [describe(t) for t in (q, k, v, log_alpha, beta, S_inout, out)]
     _check(load().kda_decode_step_t(*[_dref(d) for d in descs], _stream(stream)))
     return out
+
+
+DUMP_LAYOUT = {"g": (0, (64, 128)), "A_kk": (8192, (64, 64)), "A_qk": (12288, (64, 64)),
+               "T": (16384, (64, 64)), "U": (20480, (64, 128)), "S": (28672, (128, 128))}
+DUMP_FLOATS = 45056
+
+
+def kda_debug_chunk_dump(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, n_seqs=None,
+                         seq, head, chunk, stream=None):
+    """kda_chunk_fwd (never split) plus the intermediates of one chunk.
+
+    Returns (out, S_final, {name: tensor}) with the names of DUMP_LAYOUT."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.shape[0] - 1
+    elif n_seqs is None:
+        n_seqs = 1
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k, torch.bfloat16, "k"),
+                        (v, torch.bfloat16, "v"), (log_alpha, torch.float32, "log_alpha"),
+                        (beta, torch.float32, "beta"), (S0, torch.float32, "S0"),
+                        (cu_seqlens, torch.int32, "cu_seqlens")):
+        _require(t, dt, name)
+    out = torch.empty((T, H, dv), dtype=torch.bfloat16, device=q.device)
+    S_final = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    dump = torch.zeros(DUMP_FLOATS, dtype=torch.float32, device=q.device)
+    _check(load().kda_debug_chunk_dump(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                       _ptr(S0), _ptr(cu_seqlens), _ptr(out), _ptr(S_final), T,
+                                       n_seqs, H, dk, dv, int(seq), int(head), int(chunk),
+                                       _ptr(dump), _stream(stream)))
+    parts = {name: dump[off:off + int(np.prod(shape))].view(*shape)
+             for name, (off, shape) in DUMP_LAYOUT.items()}
+    return out, S_final, parts
 
 
 def kda_workspace_pool_bytes() -> int:

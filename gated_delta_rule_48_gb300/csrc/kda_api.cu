@@ -253,7 +253,8 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                                  float* S_final, int64_t T, int32_t N, int32_t H,
                                  int32_t dk, int32_t dv, int64_t segment_tokens, bool fused,
                                  int64_t ckpt_interval, float* ckpt, int64_t ckpt_max,
-                                 void* stream_v) {
+                                 void* stream_v, float* dump = nullptr, int32_t dump_seq = -1,
+                                 int32_t dump_head = -1, int64_t dump_chunk = -1) {
   kda_status st = check_prefill_args(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, T,
                                      N, H, dk, dv, segment_tokens, fused, ckpt_interval, ckpt,
                                      ckpt_max);
@@ -331,12 +332,16 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
     a.ckpt = ckpt_max > 0 ? ckpt : nullptr;
   }
   a.err = dev->err;
+  a.dump = dump;  // no split here: segment i is sequence i
+  a.dump_seg = dump_seq;
+  a.dump_head = dump_head;
+  a.dump_chunk = dump_chunk;
 
   kda_status result = KDA_OK;
   if (!direct) e = launch_plan(cu_seqlens, T, N, L, a.plan, a.err, s);
   if (e == cudaSuccess && split) e = launch_prefill_summary(a, s);
   if (e == cudaSuccess && split) e = launch_segment_scan(a, s);
-  if (e == cudaSuccess) e = launch_prefill_replay(a, s);
+  if (e == cudaSuccess) e = dump ? launch_prefill_replay_dump(a, s) : launch_prefill_replay(a, s);
   if (e != cudaSuccess) result = cuda_fail(e, "prefill launch");
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, s);
@@ -395,6 +400,38 @@ extern "C" kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, co
   return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
                         n_seqs, n_heads, dk, dv, 0, false, interval, checkpoints, max_checkpoints,
                         stream);
+}
+
+extern "C" kda_status kda_debug_chunk_dump(const void* q, const void* k, const void* v,
+                                           const float* log_alpha, const float* beta,
+                                           const float* S0, const int32_t* cu_seqlens, void* out,
+                                           float* S_final, int64_t total_tokens, int32_t n_seqs,
+                                           int32_t n_heads, int32_t dk, int32_t dv, int32_t seq,
+                                           int32_t head, int64_t chunk, float* dump,
+                                           void* stream) {
+  NvtxRange nvtx_range("kda_debug_chunk_dump");
+  if (!dump) return fail(KDA_ERR_INVALID_ARGUMENT, "dump is NULL");
+  if (misaligned(dump)) return fail(KDA_ERR_INVALID_ARGUMENT, "dump is not 16-byte aligned");
+  if (seq < 0 || seq >= n_seqs || head < 0 || head >= n_heads || chunk < 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "seq=%d head=%d chunk=%lld out of range", seq, head,
+                (long long)chunk);
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dump),
+                  d1 = d0 + static_cast<uintptr_t>(kDumpFloats) * sizeof(float);
+  const struct { const void* p; int64_t n; } others[] = {
+      {q, total_tokens * n_heads * dk * 2}, {k, total_tokens * n_heads * dk * 2},
+      {v, total_tokens * n_heads * dv * 2}, {log_alpha, total_tokens * n_heads * dk * 4},
+      {beta, total_tokens * n_heads * 4}, {out, total_tokens * n_heads * dv * 2},
+      {S0, S0 ? static_cast<int64_t>(n_seqs) * n_heads * dk * dv * 4 : 0},
+      {S_final, S_final ? static_cast<int64_t>(n_seqs) * n_heads * dk * dv * 4 : 0},
+      {cu_seqlens, cu_seqlens ? (static_cast<int64_t>(n_seqs) + 1) * 4 : 0}};
+  for (const auto& o : others) {
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(o.p), b1 = b0 + static_cast<uintptr_t>(o.n);
+    if (o.p && o.n > 0 && d0 < b1 && b0 < d1)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "dump overlaps another argument");
+  }
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, out, S_final, total_tokens,
+                        n_seqs, n_heads, dk, dv, -1, false, 0, nullptr, 0, stream, dump, seq,
+                        head, chunk);
 }
 
 // fused as in chunk_fwd_impl.  K tokens per sequence; commit: device [N] or null.

@@ -75,7 +75,20 @@ struct PrefillArgs {
   int fused = 0;
   const uint16_t* gate = nullptr;  // bf16 [T, H, dk] when fused
   float* ckpt = nullptr;           // f32 [ckpt_max, H, dk, dv] state checkpoints, or null
+  // intermediate dump (kda_debug_chunk_dump): the replay of segment dump_seg,
+  // head dump_head writes chunk dump_chunk's intermediates to dump (layout:
+  // the kDump* offsets below), or null
+  float* dump = nullptr;
+  int32_t dump_seg = -1, dump_head = -1;
+  int64_t dump_chunk = -1;
 };
+
+// Layout of the intermediate dump, in floats: g [64][128], A_kk [64][64],
+// A_qk [64][64], T [64][64], U [64][128], S at the chunk's start [128][128]
+// (row = key channel).
+constexpr int64_t kDumpG = 0, kDumpAkk = 64 * 128, kDumpAqk = kDumpAkk + 64 * 64,
+                  kDumpT = kDumpAqk + 64 * 64, kDumpU = kDumpT + 64 * 64,
+                  kDumpS = kDumpU + 64 * 128, kDumpFloats = kDumpS + 128 * 128;
 
 // ---- error reporting shared by the entry points (kda_api.cu)
 kda_status report_error(kda_status st, const char* msg);  // sets kda_last_error_message()
@@ -116,6 +129,8 @@ cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 // tcgen05 kernels (kda_prefill_tc.cu), dk = dv = 128 or 64
 cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
+// the replay with the intermediate dump of a.dump (one chunk of one unit)
+cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s);
 
 // ---- decode (kda_decode.cu)
 struct DecodeArgs {

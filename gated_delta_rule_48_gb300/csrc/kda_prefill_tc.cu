@@ -427,7 +427,9 @@ __device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, in
 
 // CKPT (replay only): write the state checkpoints the plan asks for; a separate
 // instantiation, so the plain replay keeps its register budget.
-template <int MODE, bool FUSED, bool CKPT>
+// DUMP (replay only): also write the intermediates of one chunk of one unit
+// (a.dump); a separate instantiation with extra barriers, for debugging.
+template <int MODE, bool FUSED, bool CKPT, bool DUMP = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -479,6 +481,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   constexpr bool kP = kOut;
   constexpr uint32_t cP = kColW;
   const int H = a.H;
+  const bool dump_unit = DUMP && seg_id == a.dump_seg && h == a.dump_head;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   uint64_t* bar_qkl = bars + 0;    // raw q, k, log_alpha of a chunk landed (TMA)
@@ -690,6 +693,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       const float4 off = *reinterpret_cast<const float4*>(sTot + warp * 128 + 4 * lane);
       const float4 gA = *reinterpret_cast<const float4*>((strip ? sG1 : sG0) + 4 * lane);
       const float2 d01 = sub2(lo2(off), lo2(gA)), d23 = sub2(hi2(off), hi2(gA));
+      if (DUMP && dump_unit && m == a.dump_chunk) {  // g = within-warp prefix + earlier warps
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(a.dump + kDumpG + (r0 + i) * 128 + 4 * lane) =
+              make_float4(g[i][0].x + off.x, g[i][0].y + off.y, g[i][1].x + off.z, g[i][1].y + off.w);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 x01 = add2(g[i][0], d01), x23 = add2(g[i][1], d23);
@@ -1069,6 +1078,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (kOut && n > 0) write_out(n - 1);
       wait_done_sync(0, n);
       if (*s_abort) break;
+      const bool dump_chunk = DUMP && dump_unit && n == a.dump_chunk;
+      if (dump_chunk) store_state(a.dump + kDumpS, 128, kColS, D);  // S at the chunk's start
 
       // ---- B: strip read-out, UT transform, T to SMEM
       {
@@ -1117,6 +1128,16 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
           }
         }
       }
+      if (dump_chunk) {  // A_kk (beta applied) and A_qk, before the inverse overwrites A_kk
+        worker_sync();
+        for (int e = tid; e < C * C; e += kWorkers) {
+          const int r = e >> 6, i = e & 63;
+          a.dump[kDumpAkk + e] = sAkk[r * kLdA + i];
+          a.dump[kDumpAqk + e] =
+              *reinterpret_cast<const float*>(R + kRAqk + sw128_offset(C, r, 4 * i));
+        }
+        worker_sync();
+      }
       // The inverse reads only the key rows (odd lane quadrants, A_kk); its
       // first step runs on warps 0 and 1.  Those nine warps meet here; the
       // query-row warps (A_qk) join at the inverse's next barrier, so their
@@ -1142,6 +1163,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         write_qeg();
       }
       if (kP) worker_sync();  // K' and the next scan start after the transform's critical step
+      if (dump_chunk) {  // T (its tf32 operand copy)
+        for (int e = tid; e < C * C; e += kWorkers) {
+          const int r = e >> 6, i = e & 63;
+          a.dump[kDumpT + e] = *reinterpret_cast<const float*>(R + kRT + sw128_offset(C, r, 4 * i));
+        }
+      }
       signal_ready(1);  // T, V (and k e^g | -P^T, q e^g) ready for group 1
 
       // ---- C: W^T = (k e^g)^T T^T (tf32), U~^T = V^T T^T (bf16 hi + lo)  ||  K' to SMEM
@@ -1166,6 +1193,14 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (kP && n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
       wait_done_sync(1, n);
       if (*s_abort) break;
+      if (dump_chunk) {  // U = T (V - k e^g S), before its tf32 rounding: U^T lanes = value channels
+        const int j = 32 * quad + lane;
+        uint32_t uv[16];
+        tmem_ld16(tmem_addr(tmem, 32 * quad, cU + 16 * part), uv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 16; ++x) a.dump[kDumpU + (16 * part + x) * 128 + j] = __uint_as_float(uv[x]);
+      }
 
       if (!kP) {  // summary: phases D and E
 
@@ -1284,7 +1319,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool FUSED, bool CKPT>
+template <int MODE, bool FUSED, bool CKPT, bool DUMP = false>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
@@ -1306,18 +1341,18 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   static int launch_regs = -1;
   if (launch_regs < 0) {
     cudaFuncAttributes fa;
-    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED, CKPT>);
+    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>);
     if (ea != cudaSuccess) return ea;
     launch_regs = fa.numRegs;
   }
   if (static_cast<uint32_t>(launch_regs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED, CKPT>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   dim3 grid(a.plan.capacity, a.H, 1);
   prof_begin(s, name);
-  prefill_tc_kernel<MODE, FUSED, CKPT><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
+  prefill_tc_kernel<MODE, FUSED, CKPT, DUMP><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
   return cudaGetLastError();
 }
@@ -1327,6 +1362,10 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
 cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s) {
   return a.fused ? launch_tc<kModeSummary, true, false>(a, s, "kda_prefill_summary")
                  : launch_tc<kModeSummary, false, false>(a, s, "kda_prefill_summary");
+}
+
+cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s) {
+  return launch_tc<kModeReplay, false, false, true>(a, s, "kda_prefill_replay_dump");
 }
 
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s) {

@@ -395,6 +395,40 @@ kda_status kda_decode_step_fused(const void *q_raw, const void *k_raw, const voi
 kda_status kda_get_device_error(void *stream);
 
 /*
+ * kda_debug_chunk_dump -- kda_chunk_fwd (never split) that also writes the
+ * intermediates of one 64-token chunk: sequence `seq`, head `head`, chunk
+ * `chunk` (0-based within the sequence).  A debugging aid: the chunked form
+ * of the recurrence goes through these steps, and comparing each with an
+ * independent evaluation locates a wrong one.  Tokens of a chunk are
+ * processed together and only the state is handed on (meridianbulletin.com
+ * article, section "Parallelizing Sequential State Updates").
+ *
+ *   dump  f32 device buffer of 45056 floats, written:
+ *         [0, 8192)        g      [64 tokens][128 key channels]: the
+ *                                 chunk-local cumulative clamped log-decay
+ *         [8192, 12288)    A_kk   [64][64]: beta_r sum_c k_rc k_ic e^{g_rc - g_ic}, i < r
+ *         [12288, 16384)   A_qk   [64][64]: sum_c q_rc k_ic e^{g_rc - g_ic}, i <= r
+ *         [16384, 20480)   T      [64][64]: (I + A_kk)^{-1} Diag(beta), as
+ *                                 the tensor core reads it (tf32)
+ *         [20480, 28672)   U      [64 tokens][128 value channels]:
+ *                                 T (V - (k e^g) S), before its tf32 rounding
+ *         [28672, 45056)   S      [128][128] (row = key channel): the state
+ *                                 at the chunk's start
+ *   Rows of tokens past the sequence's end hold the kernel's identity rows.
+ *   d = 64 runs zero-padded: channels 64..127 are zero.  Every other argument,
+ *   and out and S_final, as kda_chunk_fwd.  Slower than kda_chunk_fwd (extra
+ *   barriers in the dumping unit).  The dump must not overlap any other
+ *   argument; a chunk past the sequence's end leaves it unwritten.
+ */
+kda_status kda_debug_chunk_dump(const void *q, const void *k, const void *v,
+                                const float *log_alpha, const float *beta,
+                                const float *S0, const int32_t *cu_seqlens,
+                                void *out, float *S_final, int64_t total_tokens,
+                                int32_t n_seqs, int32_t n_heads, int32_t dk,
+                                int32_t dv, int32_t seq, int32_t head,
+                                int64_t chunk, float *dump, void *stream);
+
+/*
  * kda_workspace_pool_bytes -- memory accounting: the bytes the library's
  * workspace pool currently reserves on the current device, or -1 when the
  * library has created no pool there.  The pool is created by the first call
