@@ -157,21 +157,41 @@ void prof_end(cudaStream_t s, const char* name) {
 }
 
 // Segment length used when the caller asks for the automatic choice.
-// Splitting pays when the (sequence, head) chains alone cannot fill the GPU:
-// the summary pass costs about as much as the replay again, so split only
-// when fewer than half the SMs would be busy, and then aim at about two
-// replay units per SM.
+// Every CTA of the chunk kernels walks one (segment, head) unit at a roughly
+// fixed time per 64-token chunk, one CTA per SM, so a pass over U units of at
+// most L chunks takes about ceil(U / SMs) waves of L chunk-times.  Unsplit, the
+// N H chains take ceil(N H / SMs) waves of the whole sequence.  Split into s
+// segments per sequence, the summary pass runs the N H (s - 1) non-final units
+// and the replay all N H s units, and the scan of the entry states adds about
+// one chunk-time per segment.  Each wave also pays a fixed start (TMEM, the
+// initial state, the first chunk's loads), taken as two chunk-times.  The
+// choice is the s with the least modelled time (sequences taken as T / N
+// tokens each, at least 4 chunks per segment), and no split when splitting
+// does not beat the unsplit time.
 static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count) {
-  const int64_t chains = static_cast<int64_t>(N) * H;
-  if (T <= 0 || N <= 0) return -1;
-  if (chains * 2 >= sm_count) return -1;
-  const int64_t want_units = 2LL * sm_count;
-  const int64_t extra = want_units / H - N;  // segments beyond one per sequence
-  if (extra <= 0) return -1;
-  int64_t L = (T + extra - 1) / extra;
-  L = (L + kChunk - 1) / kChunk * kChunk;
-  L = std::max<int64_t>(L, 4 * kChunk);
-  return L;
+  if (T <= 0 || N <= 0 || H <= 0 || sm_count <= 0) return -1;
+  const int64_t chains = static_cast<int64_t>(N) * H, sms = sm_count;
+  if (chains >= sms) return -1;
+  const int64_t len = ((T + N - 1) / N + kChunk - 1) / kChunk;  // chunks per sequence
+  constexpr int64_t kWaveStart = 2, kMinChunks = 4;
+  auto waves = [&](int64_t units) { return (units + sms - 1) / sms; };
+  int64_t best = waves(chains) * (len + kWaveStart), best_L = -1;
+  for (int64_t s = 2; s <= len / kMinChunks; ++s) {
+    const int64_t L = (len + s - 1) / s;     // chunks per segment
+    const int64_t segs = (len + L - 1) / L;  // segments per sequence at that length
+    if (segs != s) continue;                 // the same cut as a smaller s
+    const int64_t t = (waves(chains * (segs - 1)) + waves(chains * segs)) * (L + kWaveStart) + segs;
+    if (t < best) {
+      best = t;
+      best_L = L;
+    }
+  }
+  return best_L > 0 ? best_L * kChunk : -1;
+}
+
+extern "C" int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
+                                           int32_t sm_count) {
+  return auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count);
 }
 
 // Host-side checks of a prefill call; nothing is launched unless all pass.

@@ -179,6 +179,24 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
                                int32_t dv, int64_t segment_tokens, void *stream);
 
 /*
+ * kda_auto_segment_tokens -- the segment length segment_tokens = 0 chooses.
+ *
+ * Host only: touches no device.  sm_count is the device's multiprocessor
+ * count (kda_chunk_fwd uses the current device's).  Returns a multiple of 64,
+ * or -1 for no split.  The choice models each chunk kernel pass as waves of
+ * one (segment, head) unit per SM: unsplit, ceil(N H / SMs) waves of the whole
+ * sequence; split into s segments per sequence, ceil(N H (s - 1) / SMs) summary
+ * waves plus ceil(N H s / SMs) replay waves of one segment, plus the scan (one
+ * chunk-time per segment) and a fixed start of two chunk-times per wave, with
+ * sequences taken as total_tokens / n_seqs tokens and segments of at least
+ * 4 chunks.  It returns the length with the least modelled time, or -1 when
+ * no split beats the unsplit pass (always when N H >= sm_count).  Invalid
+ * sizes (any of them <= 0) return -1.
+ */
+int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
+                                int32_t sm_count);
+
+/*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd without any device allocation.
  *
  * The pages have no counterpart to this entry point; it exists for callers

@@ -1,0 +1,71 @@
+"""The automatic segment length of the split prefill (kda_auto_segment_tokens,
+host only): no split when the (sequence, head) chains fill the GPU, the
+wave-filling lengths on the long-context shapes, and the documented limits."""
+import pytest
+
+from gated_delta_rule_48_gb300 import binding as kb
+
+SMS = 152
+
+
+@pytest.fixture(scope="module")
+def choose():
+    kb.build()
+    return kb.kda_auto_segment_tokens
+
+
+def test_enough_chains_means_no_split(choose):
+    assert choose(4 * 4096, 4, 32, SMS) == -1          # 128 chains, 64 chunks each
+    assert choose(152 * 65536, 152, 1, SMS) == -1      # one chain per SM
+    assert choose(1 << 20, 1, 200, SMS) == -1          # more chains than SMs
+
+
+def test_long_context_shapes(choose):
+    # 1 x 65,536 tokens, H16: 9 segments of 114 chunks -> 128 summary units and
+    # 144 replay units, one wave each
+    assert choose(65536, 1, 16, SMS) == 114 * 64
+    # 8 x 131,072 tokens, H8: 7 segments of 293 chunks -> 384 summary and 448
+    # replay units, three waves each (four segments of 547 chunks would take
+    # two waves of 547 in each pass: 2188 against 1758 chunk-times)
+    assert choose(8 * 131072, 8, 8, SMS) == 293 * 64
+
+
+def test_lengths_are_whole_chunks_and_at_least_four(choose):
+    for T, N, H in ((65536, 1, 16), (8 * 131072, 8, 8), (3 * 50000 + 1, 3, 4),
+                    (1 << 22, 2, 2), (4096, 1, 1)):
+        L = choose(T, N, H, SMS)
+        if L != -1:
+            assert L % 64 == 0 and L >= 4 * 64
+            assert L < (T + N - 1) // N  # a split cuts every sequence
+
+
+def test_short_sequences_are_not_split(choose):
+    assert choose(256, 1, 1, SMS) == -1   # 4 chunks: no two segments of 4
+    assert choose(0, 1, 1, SMS) == -1
+
+
+def test_invalid_sizes(choose):
+    for args in ((-1, 1, 1, SMS), (4096, 0, 1, SMS), (4096, 1, 0, SMS), (4096, 1, 1, 0)):
+        assert choose(*args) == -1
+
+
+def modelled(T, N, H, sms, L):
+    """Chunk-times of the split passes as kda.h documents them (L in chunks,
+    None = no split)."""
+    chains, n = N * H, -(-(-(-T // N)) // 64)
+    waves = lambda u: -(-u // sms)
+    if L is None:
+        return waves(chains) * (n + 2)
+    segs = -(-n // L)
+    return (waves(chains * (segs - 1)) + waves(chains * segs)) * (L + 2) + segs
+
+
+@pytest.mark.parametrize("T,N,H,sms", [(65536, 1, 16, 152), (8 * 131072, 8, 8, 152),
+                                       (65536, 1, 16, 76), (3 * 40000, 3, 5, 152),
+                                       (1 << 21, 1, 1, 152), (1 << 20, 2, 24, 152)])
+def test_choice_minimises_the_documented_model(choose, T, N, H, sms):
+    L = choose(T, N, H, sms)
+    got = modelled(T, N, H, sms, None if L == -1 else L // 64)
+    n = -(-(-(-T // N)) // 64)
+    others = [modelled(T, N, H, sms, c) for c in range(4, n) if -(-n // c) >= 2]
+    assert got <= min(others + [modelled(T, N, H, sms, None)])
