@@ -19,10 +19,14 @@ _CSRC = os.path.join(_PKG, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
 _BUILD = os.path.join(_PKG, "_build")
 _LIB = os.path.join(_BUILD, "libkda.so")
+# the bounds-checked build (-DKDA_BOUNDS_CHECK), objects and library apart
+_BUILD_CHECKED = os.path.join(_BUILD, "checked")
+_LIB_CHECKED = os.path.join(_BUILD_CHECKED, "libkda.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}          # False: the normal library, True: the bounds-checked one
+_checked = False    # which one load() returns
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED",
           3: "KDA_ERR_CUDA", 4: "KDA_ERR_OUT_OF_MEMORY", 5: "KDA_ERR_DEVICE_INPUT"}
@@ -35,7 +39,15 @@ class KdaError(RuntimeError):
 
 
 def library_path() -> str:
-    return _LIB
+    return _LIB_CHECKED if _checked else _LIB
+
+
+def use_checked(checked: bool) -> None:
+    """Route every call of this module to the bounds-checked library (True)
+    or to the normal one (False, the default).  Both may be loaded at once;
+    each keeps its own device state."""
+    global _checked
+    _checked = bool(checked)
 
 
 def _sources():
@@ -47,22 +59,27 @@ def _headers():
     return hs + [os.path.join(_INCLUDE, "kda.h")]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every ``csrc/*.cu`` for sm_103a and link ``_build/libkda.so``.
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile every ``csrc/*.cu`` for sm_103a and link ``_build/libkda.so``
+    (with ``checked``: ``_build/checked/libkda.so``, every kernel compiled with
+    -DKDA_BOUNDS_CHECK).
 
     Translation units compile in parallel; nvcc cross-compiles, so no GPU is
     needed.  Rebuilds only when a source or header is newer than the library.
     """
-    os.makedirs(_BUILD, exist_ok=True)
+    bdir, lib_path = (_BUILD_CHECKED, _LIB_CHECKED) if checked else (_BUILD, _LIB)
+    os.makedirs(bdir, exist_ok=True)
     srcs = _sources()
     newest = max(os.path.getmtime(p) for p in srcs + _headers())
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
-        return _LIB
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= newest:
+        return lib_path
     common = ["nvcc", *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", _INCLUDE, "-I", _CSRC, "--expt-relaxed-constexpr"]
+    if checked:
+        common.append("-DKDA_BOUNDS_CHECK")
     objs, procs = [], []
     for src in srcs:
-        obj = os.path.join(_BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         cmd = common + ["-c", src, "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE,
@@ -76,10 +93,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(" ".join(cmd))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = _LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.check_call(["nvcc", *ARCH_FLAGS, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 class KdaTensor(ctypes.Structure):
@@ -113,10 +130,11 @@ class _KernelTime(ctypes.Structure):
 
 def load():
     """Load (building first if needed) the library; returns the ctypes handle."""
-    global _lib
     with _lock:
-        if _lib is None:
-            path = _LIB if os.path.exists(_LIB) else build()
+        if _checked not in _libs:
+            path = library_path()
+            if not os.path.exists(path):
+                path = build(checked=_checked)
             lib = ctypes.CDLL(path)
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
             lib.kda_chunk_fwd.restype = ctypes.c_int
@@ -161,12 +179,16 @@ def load():
                                                     ctypes.c_int32]
             lib.kda_selftest_bounded_wait.restype = ctypes.c_int
             lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
+            lib.kda_selftest_bounds_check.restype = ctypes.c_int
+            lib.kda_selftest_bounds_check.argtypes = [vp]
+            lib.kda_bounds_checked.restype = ctypes.c_int
+            lib.kda_bounds_checked.argtypes = []
             lib.kda_profile_enable.restype = None
             lib.kda_profile_enable.argtypes = [ctypes.c_int]
             lib.kda_profile_read.restype = ctypes.c_int
             lib.kda_profile_read.argtypes = [ctypes.POINTER(_KernelTime), ctypes.c_int]
-            _lib = lib
-    return _lib
+            _libs[_checked] = lib
+    return _libs[_checked]
 
 
 def _check(status: int):
@@ -358,6 +380,16 @@ def kda_workspace_pool_bytes() -> int:
 def kda_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return load().kda_get_device_error(_stream(stream))
+
+
+def kda_bounds_checked() -> bool:
+    """Whether the loaded library is the bounds-checked build."""
+    return bool(load().kda_bounds_checked())
+
+
+def kda_selftest_bounds_check(*, stream=None):
+    """One out-of-range guard, no memory access (see include/kda.h)."""
+    _check(load().kda_selftest_bounds_check(_stream(stream)))
 
 
 def kda_selftest_bounded_wait(polls: int = 1000, *, stream=None):

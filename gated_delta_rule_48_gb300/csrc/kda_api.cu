@@ -569,6 +569,8 @@ extern "C" kda_status kda_get_device_error(void* stream) {
   if (word & kDevErrCommit) msg += "a decode commit count is outside [0, n_tokens]; ";
   if (word & kDevErrCheckpoints)
     msg += "the sequences have more checkpoints than max_checkpoints (the excess was dropped); ";
+  if (word & kDevErrBounds)
+    msg += "a kernel index fell outside its buffer (bounds-checked build; the access was skipped); ";
   return fail(KDA_ERR_DEVICE_INPUT, "%s", msg.c_str());
 }
 
@@ -584,6 +586,18 @@ extern "C" kda_status kda_selftest_bounded_wait(uint32_t polls, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return KDA_OK;
 }
+
+extern "C" kda_status kda_selftest_bounds_check(void* stream) {
+  NvtxRange nvtx_range("kda_selftest_bounds_check");
+  DeviceState* dev = nullptr;
+  kda_status st = device_state(&dev);
+  if (st != KDA_OK) return st;
+  const cudaError_t e = launch_bounds_guard_selftest(dev->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return KDA_OK;
+}
+
+extern "C" int kda_bounds_checked(void) { return kBoundsChecked ? 1 : 0; }
 
 extern "C" int64_t kda_workspace_pool_bytes(void) {
   int dev = 0;

@@ -57,9 +57,12 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   const int64_t n = unit / H, h = unit % H;
   const int tid = threadIdx.x;
   const int cg = tid % CG, rg = tid / CG;
+  // extents (bounds-checked build): units = N H, tokens = N K
+  const int64_t units = gridDim.x, n_tok_h = units * K;
 
   int n_commit = K;
   if (commit) {
+    if (!kda_guard(n, 1, units / H, err)) return;
     n_commit = commit[n];
     if (n_commit < 0 || n_commit > K) {  // rejected: nothing is written for this unit
       if (tid == 0) atomicOr(err, kDevErrCommit);
@@ -77,7 +80,10 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   float4* Sp = reinterpret_cast<float4*>(S + unit * D * D);
   float4 st[RPT];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) st[i] = __ldcs(&Sp[(rg * RPT + i) * CG + cg]);
+  for (int i = 0; i < RPT; ++i)
+    st[i] = kda_guard(unit * D * D + 4 * ((rg * RPT + i) * CG + cg), 4, units * D * D, err)
+                ? __ldcs(&Sp[(rg * RPT + i) * CG + cg])
+                : make_float4(0.f, 0.f, 0.f, 0.f);
 
   // Token t's vectors are loaded into registers (thread c < D: channel c)
   // while token t-1 is computed, so their latency is hidden after the first.
@@ -87,14 +93,14 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
   float pla = 0.f, pb = 0.f;
   auto fetch = [&](int t) {
     const int64_t row = (n * K + t) * H + h;
-    if (chan) {
+    if (chan && kda_guard(row * D + tid, 1, n_tok_h * D, err)) {
       const int64_t e = row * D + tid;
       pk = k[e];
       pq = q[e];
       pv = v[e];
       if (FUSED) pg = gate[e]; else pla = log_alpha[e];
     }
-    pb = beta[row];
+    if (kda_guard(row, 1, n_tok_h, err)) pb = beta[row];
   };
   fetch(0);
 
@@ -154,7 +160,7 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
       for (int r = 0; r < RG; ++r) { sa += s_red_a[r][col]; sb += s_red_b[r][col]; }
       const float u = bt * (vt - sa);
       s_u[col] = u;
-      out[vec + col] = f32_to_bf16(sb + s_qk * u);
+      if (kda_guard(vec + col, 1, n_tok_h * D, err)) out[vec + col] = f32_to_bf16(sb + s_qk * u);
     }
     __syncthreads();
 
@@ -166,7 +172,9 @@ decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     }
     if (t + 1 == n_commit) {
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) __stcs(&Sp[(rg * RPT + i) * CG + cg], st[i]);
+      for (int i = 0; i < RPT; ++i)
+        if (kda_guard(unit * D * D + 4 * ((rg * RPT + i) * CG + cg), 4, units * D * D, err))
+          __stcs(&Sp[(rg * RPT + i) * CG + cg], st[i]);
     }
     if (t + 1 < K) __syncthreads();  // s_k, s_q, s_u are rewritten by the next token
   }

@@ -68,6 +68,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The state of unit u into shared memory; in the bounds-checked build a copy
+// whose source range is outside the state buffer is not issued, and a plain
+// arrival completes the phase instead (the unit then computes from stale data,
+// and the device error word reports the violation)
+template <int D>
+__device__ __forceinline__ void fetch_state(float* dst, float* S, int64_t u, int64_t units,
+                                            uint64_t* bar, int* err) {
+  if (kda_guard(u * D * D, static_cast<int64_t>(D) * D, units * D * D, err))
+    bulk_load(dst, S + u * D * D, static_cast<uint32_t>(D * D * 4), bar);
+  else
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Bounded wait on the mbarrier phase `parity`: false after `limit` polls (each
 // poll blocks for a hardware-chosen interval), never an endless spin.
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity,
@@ -157,8 +170,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
   }
   __syncthreads();
   int64_t unit = blockIdx.x;  // sequence * H + head
-  if (tid == 0 && unit < units)
-    bulk_load(s_state, S + unit * D * D, static_cast<uint32_t>(Cfg::kStateBytes), bar);
+  if (tid == 0 && unit < units) fetch_state<D>(s_state, S, unit, units, bar, err);
   uint32_t parity = 0;
 
 #pragma unroll 1
@@ -180,12 +192,12 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
     }
     if (tid == 0 && unit + stride < units) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      bulk_load(s_state, S + (unit + stride) * D * D, static_cast<uint32_t>(Cfg::kStateBytes),
-                bar);
+      fetch_state<D>(s_state, S, unit + stride, units, bar, err);
     }
 
     int n_commit = K;
     if (commit) {
+      if (!kda_guard(n, 1, units / H, err)) continue;
       n_commit = commit[n];
       if (n_commit < 0 || n_commit > K) {  // rejected: nothing is written for this unit
         if (tid == 0) atomicOr(err, kDevErrCommit);
@@ -204,6 +216,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
         constexpr int PER = D / 32;  // channels per lane: lane * PER .. + PER - 1 (4 or 2)
         float kf[PER], qf[PER], al[PER], vf[PER];
         const int64_t e0 = row * D + lane * PER;  // one vector load per input
+        if (!kda_guard(e0, PER, units * K * D, err)) continue;  // warp-uniform
         load_bf16<PER>(k + e0, kf);
         load_bf16<PER>(q + e0, qf);
         load_bf16<PER>(v + e0, vf);
@@ -246,7 +259,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
         for (int o = 16; o; o >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o);
         if (lane == 0) {
           s_qk[tt] = qk;
-          s_beta[tt] = beta[row];
+          s_beta[tt] = kda_guard(row, 1, units * K, err) ? beta[row] : 0.f;
         }
       }
       __syncthreads();
@@ -300,7 +313,7 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
           a0 += pa.x; a1 += pa.y; b0 += pb.x; b1 += pb.y;
         }
         const float u0 = s_beta[tt] * (vt.x - a0), u1 = s_beta[tt] * (vt.y - a1);
-        if (quarter == 0)
+        if (quarter == 0 && kda_guard(row * D + j, 2, units * K * D, err))
           *reinterpret_cast<uint32_t*>(out + row * D + j) =
               static_cast<uint32_t>(f32_to_bf16(b0 + s_qk[tt] * u0)) |
               (static_cast<uint32_t>(f32_to_bf16(b1 + s_qk[tt] * u1)) << 16);
@@ -320,8 +333,10 @@ decode_tokens_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict_
             const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
             for (int x = 0; x < 4; ++x)
-              __stcs(reinterpret_cast<float2*>(Sc + static_cast<int64_t>(i + x) * D),
-                     __fmul2_rn(st[i + x], make_float2(pv[x], pv[x])));
+              if (kda_guard(unit * D * D + static_cast<int64_t>(quarter * RPT + i + x) * D + j, 2,
+                            units * D * D, err))
+                __stcs(reinterpret_cast<float2*>(Sc + static_cast<int64_t>(i + x) * D),
+                       __fmul2_rn(st[i + x], make_float2(pv[x], pv[x])));
           }
         }
       }

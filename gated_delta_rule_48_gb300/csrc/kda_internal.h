@@ -26,7 +26,29 @@ enum DeviceError : int {
   kDevErrTimeout = 4,        // a kernel gave up waiting on its own async copies / MMAs
   kDevErrCommit = 8,         // a decode commit count outside [0, tokens per call]
   kDevErrCheckpoints = 16,   // more prefill checkpoints than the caller's buffer holds
+  kDevErrBounds = 32,        // bounds-checked build: an index fell outside its buffer
 };
+
+// ---- bounds-checked build.  Compiled with -DKDA_BOUNDS_CHECK, every plain
+// global-memory access of the kernels (the TMA copies check their own boxes
+// against the tensor maps) first asks kda_guard whether elements
+// [i, i + width) lie inside a buffer of n elements.  Out of range, the access
+// is skipped and kDevErrBounds is set in the device error word: the kernel
+// never traps and never touches memory it does not own.  Without the flag the
+// guard is the constant true and the checks compile away.
+#ifdef KDA_BOUNDS_CHECK
+constexpr bool kBoundsChecked = true;
+__device__ __forceinline__ bool kda_guard(int64_t i, int64_t width, int64_t n, int* err) {
+  if (i >= 0 && width >= 0 && i + width <= n) return true;
+  atomicOr(err, kDevErrBounds);
+  return false;
+}
+#else
+constexpr bool kBoundsChecked = false;
+__device__ __forceinline__ constexpr bool kda_guard(int64_t, int64_t, int64_t, int*) {
+  return true;
+}
+#endif
 
 // One segment of one sequence: tokens [t0, t1) (global indices).
 struct Segment {
@@ -151,6 +173,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tokens(const DecodeArgs& a, cudaStream_t s);
 // kda_selftest.cu: a bounded wait on an mbarrier nothing arrives on
 cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, cudaStream_t s);
+// kda_selftest.cu: one out-of-range bounds guard (records kDevErrBounds only in
+// the bounds-checked build; accesses no memory in either build)
+cudaError_t launch_bounds_guard_selftest(int* err, cudaStream_t s);
 
 // bf16 helpers usable from device code without cuda_bf16.h conversions.
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {

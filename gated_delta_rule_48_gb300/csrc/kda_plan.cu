@@ -39,9 +39,11 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
 
   // 1. validate cu_seqlens
   if (cu) {
-    if (tid == 0 && (cu[0] != 0 || static_cast<int64_t>(cu[N]) != T)) atomicOr(&s_bad, 1);
+    if (tid == 0 && kda_guard(N, 1, static_cast<int64_t>(N) + 1, err) &&
+        (cu[0] != 0 || static_cast<int64_t>(cu[N]) != T))
+      atomicOr(&s_bad, 1);
     for (int n = tid; n < N; n += kPlanThreads)
-      if (cu[n + 1] < cu[n]) atomicOr(&s_bad, 1);
+      if (kda_guard(n, 2, static_cast<int64_t>(N) + 1, err) && cu[n + 1] < cu[n]) atomicOr(&s_bad, 1);
   }
   __syncthreads();
   if (s_bad) {
@@ -55,7 +57,7 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
     const int n = base + tid;
     int64_t t0 = 0, len = 0;
     int32_t cnt = 0;
-    if (n < N) {
+    if (n < N && (!cu || kda_guard(n, 2, static_cast<int64_t>(N) + 1, err))) {
       t0 = cu ? cu[n] : uni * n;
       len = cu ? static_cast<int64_t>(cu[n + 1]) - cu[n] : uni;
       cnt = 1;
@@ -73,7 +75,7 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
       s_cscan[tid] += cadd;
       __syncthreads();
     }
-    if (n < N && CI > 0) plan.ckpt_base[n] = s_cbase + s_cscan[tid] - ccnt;
+    if (n < N && CI > 0 && kda_guard(n, 1, N, err)) plan.ckpt_base[n] = s_cbase + s_cscan[tid] - ccnt;
     const int32_t first = s_base + s_scan[tid] - cnt;
     if (n < N) {
       for (int32_t j = 0; j < cnt; ++j) {
@@ -86,7 +88,7 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
         sg.index = j;
         sg.count = cnt;
         sg.first = first;
-        plan.segs[id] = sg;
+        if (kda_guard(id, 1, plan.capacity, err)) plan.segs[id] = sg;
       }
     }
     __syncthreads();
@@ -148,9 +150,10 @@ segment_scan_kernel(PrefillArgs a) {
     int lo = 0, hi = n_segs;
     while (lo < hi) {
       int mid = (lo + hi) >> 1;
+      if (!kda_guard(mid, 1, a.plan.capacity, a.err)) break;
       if (a.plan.segs[mid].seq < n) lo = mid + 1; else hi = mid;
     }
-    if (lo < n_segs && a.plan.segs[lo].seq == n) {
+    if (lo < n_segs && kda_guard(lo, 1, a.plan.capacity, a.err) && a.plan.segs[lo].seq == n) {
       s_first = lo;
       s_count = a.plan.segs[lo].count;
     }
@@ -161,32 +164,40 @@ segment_scan_kernel(PrefillArgs a) {
   // (64 runs zero-padded to 128)
   const int W = 2 * D;  // width of the B | M record
   const int DIO = a.dv;
-  auto rec_of = [&](int64_t seg) {
-    return a.incr_trans + (seg * a.H + h) * static_cast<int64_t>(D) * W;
-  };
-  auto stage_M = [&](int buf, const float* rec) {  // M_j -> sm.M[buf], 16 bytes per copy
+  // element offset of segment seg's record in incr_trans (n_it floats), and
+  // the entry states' extent
+  auto rec_off = [&](int64_t seg) { return (seg * a.H + h) * static_cast<int64_t>(D) * W; };
+  const int64_t n_it = static_cast<int64_t>(a.plan.capacity) * a.H * D * W;
+  const int64_t n_es = static_cast<int64_t>(a.plan.capacity) * a.H * D * D;
+  auto stage_M = [&](int buf, int64_t off) {  // M_j -> sm.M[buf], 16 bytes per copy
     for (int i = tid; i < D * (D / 4); i += kScanThreads) {
       const int c = i / (D / 4), m4 = i % (D / 4);
-      cp_async16(&sm.M[buf][c * LD + 4 * m4], rec + static_cast<int64_t>(c) * W + D + 4 * m4);
+      const int64_t e = off + static_cast<int64_t>(c) * W + D + 4 * m4;
+      if (kda_guard(e, 4, n_it, a.err)) cp_async16(&sm.M[buf][c * LD + 4 * m4], a.incr_trans + e);
     }
     cp_async_commit();
   };
-  stage_M(0, rec_of(s_first));
+  stage_M(0, rec_off(s_first));
   for (int i = tid; i < D * kScanCols; i += kScanThreads) {
     const int c = i / kScanCols, j = i % kScanCols;
-    sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO)
-                  ? a.S0[((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j]
+    const int64_t e = ((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j;
+    sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO &&
+               kda_guard(e, 1, static_cast<int64_t>(a.N) * a.H * DIO * DIO, a.err))
+                  ? a.S0[e]
                   : 0.f;
   }
   const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + 32 r
   for (int sgi = 0; sgi + 1 < s_count; ++sgi) {
     const int64_t seg = s_first + sgi;
-    const float* rec = rec_of(seg);
+    const int64_t roff = rec_off(seg);
     float acc[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) acc[r] = rec[static_cast<int64_t>(c0 + 32 * r) * W + col0 + j];  // B_j
+    for (int r = 0; r < RPT; ++r) {  // B_j
+      const int64_t e = roff + static_cast<int64_t>(c0 + 32 * r) * W + col0 + j;
+      acc[r] = kda_guard(e, 1, n_it, a.err) ? a.incr_trans[e] : 0.f;
+    }
     if (sgi + 2 < s_count) {  // stage the next transition while this one is used
-      stage_M((sgi + 1) & 1, rec_of(seg + 1));
+      stage_M((sgi + 1) & 1, rec_off(seg + 1));
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
@@ -204,8 +215,9 @@ segment_scan_kernel(PrefillArgs a) {
     for (int r = 0; r < RPT; ++r) {
       const int c = c0 + 32 * r;
       sm.S[c * kScanCols + j] = acc[r];
-      a.entry_state[((seg + 1) * a.H + h) * static_cast<int64_t>(D) * D +
-                    static_cast<int64_t>(c) * D + col0 + j] = acc[r];
+      const int64_t e = ((seg + 1) * a.H + h) * static_cast<int64_t>(D) * D +
+                        static_cast<int64_t>(c) * D + col0 + j;
+      if (kda_guard(e, 1, n_es, a.err)) a.entry_state[e] = acc[r];
     }
     __syncthreads();
   }

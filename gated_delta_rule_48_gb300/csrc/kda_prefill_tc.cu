@@ -450,7 +450,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     sg.count = 1;
     sg.first = seg_id;
   } else {
-    if (seg_id >= *a.plan.n_segs) return;
+    if (seg_id >= *a.plan.n_segs || !kda_guard(seg_id, 1, a.plan.capacity, a.err)) return;
     sg = a.plan.segs[seg_id];
   }
   const bool last = sg.index + 1 == sg.count;
@@ -578,17 +578,26 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   };
 
   float beta_reg = 0.f;  // beta of the next chunk to be scanned (threads < 64)
-  if (tid < C && sg.t0 + tid < sg.t1) beta_reg = a.beta[(sg.t0 + tid) * H + h];
+  if (tid < C && sg.t0 + tid < sg.t1 && kda_guard((sg.t0 + tid) * H + h, 1, a.T * H, a.err))
+    beta_reg = a.beta[(sg.t0 + tid) * H + h];
 
   // ---- initial state, transposed into TMEM: S^T[j][c] = S_init[c][j] (worker warps)
   if (warp < kWarps) {
     const int j = 32 * quad + lane;
-    const float* src = nullptr;
+    const float* src = nullptr;  // buffer src_buf (src_n floats) at offset src_off
+    const float* src_buf = nullptr;
+    int64_t src_off = 0, src_n = 0;
     if (MODE == kModeReplay) {
-      if (sg.index == 0)
-        src = a.S0 ? a.S0 + (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO : nullptr;
-      else
-        src = a.entry_state + (static_cast<int64_t>(seg_id) * H + h) * D * D;
+      if (sg.index == 0) {
+        src_buf = a.S0;
+        src_off = (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO;
+        src_n = static_cast<int64_t>(a.N) * H * DIO * DIO;
+      } else {
+        src_buf = a.entry_state;
+        src_off = (static_cast<int64_t>(seg_id) * H + h) * D * D;
+        src_n = static_cast<int64_t>(a.plan.capacity) * H * D * D;
+      }
+      if (src_buf) src = src_buf + src_off;
     }
     const int lds = (MODE == kModeReplay && sg.index == 0) ? DIO : D;  // row stride of src
 #pragma unroll
@@ -597,7 +606,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         const int c = 32 * part + cc + x;
-        r[x] = __float_as_uint(src && c < lds && j < lds ? src[c * lds + j] : 0.f);
+        r[x] = __float_as_uint(
+            src && c < lds && j < lds && kda_guard(src_off + c * lds + j, 1, src_n, a.err)
+                ? src[c * lds + j]
+                : 0.f);
       }
       tmem_st16(tmem_addr(tmem, 32 * quad, kColS + 32 * part + cc), r);
       if (kSum) {  // S_M = I
@@ -685,7 +697,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     }
     if (tid < C) {
       const int64_t t = sg.t0 + (m + 1) * C + tid;
-      beta_reg = t < sg.t1 ? a.beta[t * H + h] : 0.f;
+      beta_reg = t < sg.t1 && kda_guard(t * H + h, 1, a.T * H, a.err) ? a.beta[t * H + h] : 0.f;
     }
     worker_sync();
     {
@@ -696,8 +708,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (DUMP && dump_unit && m == a.dump_chunk) {  // g = within-warp prefix + earlier warps
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(a.dump + kDumpG + (r0 + i) * 128 + 4 * lane) =
-              make_float4(g[i][0].x + off.x, g[i][0].y + off.y, g[i][1].x + off.z, g[i][1].y + off.w);
+          if (kda_guard(kDumpG + (r0 + i) * 128 + 4 * lane, 4, kDumpFloats, a.err))
+            *reinterpret_cast<float4*>(a.dump + kDumpG + (r0 + i) * 128 + 4 * lane) = make_float4(
+                g[i][0].x + off.x, g[i][0].y + off.y, g[i][1].x + off.z, g[i][1].y + off.w);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -771,14 +784,16 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
       const int t = 16 * part + 2 * y + (odd ? 1 : 0);
       const float lo = odd ? recv : v0, hi = odd ? v1 : recv;
-      if (t < valid && j < DIO)
+      if (t < valid && j < DIO &&
+          kda_guard(((c0 + t) * H + h) * DIO + (j & ~1), 2, a.T * H * DIO, a.err))
         *reinterpret_cast<uint32_t*>(a.out + ((c0 + t) * H + h) * DIO + (j & ~1)) = pack_bf16x2(lo, hi);
     }
   };
 
-  // S^T (TMEM) -> dst[c * ld + j] = S[c][j] (row = key channel), f32; worker warps.
-  // rows and columns below lim of the state in TMEM columns col.. to dst
-  auto store_state = [&](float* dst, int64_t ld, uint32_t col, int lim) {
+  // S^T (TMEM) -> buf[off + c * ld + j] = S[c][j] (row = key channel), f32, in a
+  // buffer of n floats; worker warps.  Rows and columns below lim of the state
+  // in TMEM columns col..
+  auto store_state = [&](float* buf, int64_t off, int64_t n, int64_t ld, uint32_t col, int lim) {
     const int j = 32 * quad + lane;
 #pragma unroll
     for (int cc = 0; cc < 32; cc += 16) {
@@ -787,7 +802,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       tmem_wait_ld();
       if (j < lim && 32 * part + cc < lim) {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dst[(32 * part + cc + x) * ld + j] = __uint_as_float(sv[x]);
+        for (int x = 0; x < 16; ++x) {
+          const int64_t e = off + (32 * part + cc + x) * ld + j;
+          if (kda_guard(e, 1, n, a.err)) buf[e] = __uint_as_float(sv[x]);
+        }
       }
     }
   };
@@ -1079,7 +1097,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       wait_done_sync(0, n);
       if (*s_abort) break;
       const bool dump_chunk = DUMP && dump_unit && n == a.dump_chunk;
-      if (dump_chunk) store_state(a.dump + kDumpS, 128, kColS, D);  // S at the chunk's start
+      if (dump_chunk) store_state(a.dump, kDumpS, kDumpFloats, 128, kColS, D);  // S at the chunk's start
 
       // ---- B: strip read-out, UT transform, T to SMEM
       {
@@ -1132,9 +1150,11 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         worker_sync();
         for (int e = tid; e < C * C; e += kWorkers) {
           const int r = e >> 6, i = e & 63;
-          a.dump[kDumpAkk + e] = sAkk[r * kLdA + i];
-          a.dump[kDumpAqk + e] =
-              *reinterpret_cast<const float*>(R + kRAqk + sw128_offset(C, r, 4 * i));
+          if (kda_guard(kDumpAqk + e, 1, kDumpFloats, a.err)) {
+            a.dump[kDumpAkk + e] = sAkk[r * kLdA + i];
+            a.dump[kDumpAqk + e] =
+                *reinterpret_cast<const float*>(R + kRAqk + sw128_offset(C, r, 4 * i));
+          }
         }
         worker_sync();
       }
@@ -1166,7 +1186,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (dump_chunk) {  // T (its tf32 operand copy)
         for (int e = tid; e < C * C; e += kWorkers) {
           const int r = e >> 6, i = e & 63;
-          a.dump[kDumpT + e] = *reinterpret_cast<const float*>(R + kRT + sw128_offset(C, r, 4 * i));
+          if (kda_guard(kDumpT + e, 1, kDumpFloats, a.err))
+            a.dump[kDumpT + e] = *reinterpret_cast<const float*>(R + kRT + sw128_offset(C, r, 4 * i));
         }
       }
       signal_ready(1);  // T, V (and k e^g | -P^T, q e^g) ready for group 1
@@ -1199,7 +1220,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         tmem_ld16(tmem_addr(tmem, 32 * quad, cU + 16 * part), uv);
         tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) a.dump[kDumpU + (16 * part + x) * 128 + j] = __uint_as_float(uv[x]);
+        for (int x = 0; x < 16; ++x)
+          if (kda_guard(kDumpU + (16 * part + x) * 128 + j, 1, kDumpFloats, a.err))
+            a.dump[kDumpU + (16 * part + x) * 128 + j] = __uint_as_float(uv[x]);
       }
 
       if (!kP) {  // summary: phases D and E
@@ -1238,12 +1261,18 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
       if (CKPT) {  // the state after this chunk, if the sequence has a checkpoint here
         // tokens of the sequence up to this chunk's end (< 2^31: TMA coordinates are 32-bit)
         const int32_t ci = static_cast<int32_t>(a.plan.ckpt_interval);
-        const int32_t pos = static_cast<int32_t>(sg.t0 - a.plan.segs[sg.first].t0) +
-                            static_cast<int32_t>(n) * C + chunk_valid(n);
-        if (pos % ci == 0) {
+        const bool refs_ok = kda_guard(sg.first, 1, a.plan.capacity, a.err) &&
+                             kda_guard(sg.seq, 1, a.N, a.err);
+        const int32_t pos =
+            refs_ok ? static_cast<int32_t>(sg.t0 - a.plan.segs[sg.first].t0) +
+                          static_cast<int32_t>(n) * C + chunk_valid(n)
+                    : 1;
+        if (refs_ok && pos % ci == 0) {
           const int64_t slot = a.plan.ckpt_base[sg.seq] + pos / ci - 1;
           if (slot < a.plan.ckpt_max) {  // 8 columns at a time: few live registers mid-loop
-            float* dst = a.ckpt + (slot * H + h) * DIO * DIO;
+            const int64_t ck_off = (slot * H + h) * DIO * DIO;
+            const int64_t ck_n = a.plan.ckpt_max * H * DIO * DIO;
+            float* dst = a.ckpt + ck_off;
             const int j = 32 * quad + lane;
 #pragma unroll 1
             for (int cc = 0; cc < 32; cc += 8) {
@@ -1253,7 +1282,8 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
               if (j < DIO && 32 * part + cc < DIO) {
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
-                  dst[(32 * part + cc + x) * DIO + j] = __uint_as_float(sv[x]);
+                  if (kda_guard(ck_off + (32 * part + cc + x) * DIO + j, 1, ck_n, a.err))
+                    dst[(32 * part + cc + x) * DIO + j] = __uint_as_float(sv[x]);
               }
             }
           }
@@ -1267,11 +1297,13 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     if (!*s_abort) {
       if (MODE == kModeReplay) {
         if (last && a.S_final)
-          store_state(a.S_final + (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO, DIO, kColS, DIO);
+          store_state(a.S_final, (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO,
+                      static_cast<int64_t>(a.N) * H * DIO * DIO, DIO, kColS, DIO);
       } else {  // the increment | transition record, rows of 2 D floats
-        float* dst = a.incr_trans + (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D);
-        store_state(dst, 2 * D, kColS, D);
-        store_state(dst + D, 2 * D, cSM, D);
+        const int64_t off = (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D);
+        const int64_t n_it = static_cast<int64_t>(a.plan.capacity) * H * D * (2 * D);
+        store_state(a.incr_trans, off, n_it, 2 * D, kColS, D);
+        store_state(a.incr_trans, off + D, n_it, 2 * D, cSM, D);
       }
     }
   }  // worker warps

@@ -5,6 +5,10 @@
 // kernel takes, instead of spinning forever, if its copies or MMAs never
 // complete; the test shows the status reaches the host and the context stays
 // usable, without faulting or hanging the GPU.
+// Self-test of the bounds guard: one guard on element 1 of a one-element
+// buffer, and no memory access at all.  In the bounds-checked build it
+// records kDevErrBounds; in the normal build the guard is compiled out and the
+// kernel does nothing, so the test tells which build is loaded.
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -24,7 +28,16 @@ __global__ void bounded_wait_kernel(uint32_t polls, int* err) {
   if (threadIdx.x == 0 && !sm100::mbar_wait(&bar, 0, polls)) atomicOr(err, kDevErrTimeout);
 }
 
+__global__ void bounds_guard_kernel(int* err) {
+  if (threadIdx.x == 0) (void)kda_guard(1, 1, 1, err);
+}
+
 }  // namespace
+
+cudaError_t launch_bounds_guard_selftest(int* err, cudaStream_t s) {
+  bounds_guard_kernel<<<1, 32, 0, s>>>(err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, cudaStream_t s) {
   bounded_wait_kernel<<<1, 32, 0, s>>>(polls, err);

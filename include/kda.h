@@ -478,6 +478,24 @@ int kda_abi_version(void);
 kda_status kda_selftest_bounded_wait(uint32_t polls, void *stream);
 
 /*
+ * The bounds-checked build.  Compiled with -DKDA_BOUNDS_CHECK (the binding's
+ * build(checked=True) makes _build/checked/libkda.so), every plain
+ * global-memory load and store of the kernels first checks that its elements
+ * lie inside the buffer they index (extents from the call's sizes); an access
+ * outside is skipped and recorded in the device error word, which the next
+ * kda_get_device_error returns as KDA_ERR_DEVICE_INPUT naming the violation.
+ * No kernel traps.  TMA copies are bounded by their tensor maps in both builds.
+ *
+ * kda_bounds_checked -- 1 in the bounds-checked build, 0 otherwise (host only).
+ * kda_selftest_bounds_check -- launch, on `stream`, one guard on an index
+ * outside a one-element buffer, with no memory access: afterwards
+ * kda_get_device_error reports the violation in the bounds-checked build and
+ * KDA_OK in the normal one.
+ */
+int kda_bounds_checked(void);
+kda_status kda_selftest_bounds_check(void *stream);
+
+/*
  * Launch timing (tracing aid).  While enabled, every kernel the library
  * launches is bracketed by CUDA events on its launch stream.
  * kda_profile_read() synchronises the device, then reports per kernel name
