@@ -663,7 +663,6 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
                          ? *reinterpret_cast<const uint2*>(sm + kRawQ + sw128_offset(C, r, 8 * lane))
                          : make_uint2(0u, 0u);
       }
-      if (FUSED) l2norm8_bf16(cr.kraw, cr.qraw, lane);  // q, k of the warp's 4 tokens
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_raw);  // this warp is done with the raw tiles
       *reinterpret_cast<float4*>(sTot + warp * 128 + 4 * lane) =
@@ -1086,6 +1085,7 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     if (n_chunks > 0) {
       scan_chunk(0);
       worker_sync();
+      if (FUSED) l2norm8_bf16(cr.kraw, cr.qraw, lane);  // q, k of the warp's 4 tokens
       build_chunk();
       signal_ready(0);  // strip operands of chunk 0
     }
@@ -1254,6 +1254,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
 
       // ---- G: O^T += U^T A_qk^T ; S^T += U^T K'  (A = U^T)  ||  chunk n+1 operand build
       if (n + 1 < n_chunks) {
+        // fused preparation: L2-normalise chunk n+1's q and k here, beside the
+        // state MMAs, rather than in its decay scan, which sits on the path
+        // of phase C
+        if (FUSED) l2norm8_bf16(cr.kraw, cr.qraw, lane);
         build_chunk();  // chunk n+1 operands into freed buffers
         signal_ready(0);
       }
