@@ -292,6 +292,9 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   if (!split) L = -1;
   const int64_t capacity64 = split ? static_cast<int64_t>(N) + (T + L - 1) / L + 1 : N;
   if (capacity64 > (1LL << 30)) return fail(KDA_ERR_UNSUPPORTED, "too many segments");
+  if (capacity64 * H > 0x7fffffffLL)  // one block per (segment, head) unit
+    return fail(KDA_ERR_UNSUPPORTED, "%lld segments x %d heads exceed the grid",
+                (long long)capacity64, H);
   const int32_t capacity = static_cast<int32_t>(capacity64);
 
   // workspace: [segment count | segments | incr_trans | entry_state]
@@ -306,7 +309,8 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   const bool want_ckpt = ckpt_interval > 0;  // the planner counts (and flags an overflow) even if max = 0
   size_t off_ck = align_up(off_es + es_bytes);
   size_t ck_base_bytes = want_ckpt ? sizeof(int64_t) * (size_t)N : 0;
-  size_t ws_bytes = align_up(off_ck + ck_base_bytes);
+  size_t off_ord = align_up(off_ck + ck_base_bytes);  // launch order, longest segment first
+  size_t ws_bytes = align_up(off_ord + sizeof(int32_t) * capacity);
 
   // A uniform batch with neither split nor checkpoints needs no plan and no
   // workspace: the chunk kernel takes segment i = sequence i.
@@ -344,6 +348,7 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.plan.segs = direct ? nullptr : reinterpret_cast<Segment*>(ws + off_segs);
   a.plan.n_segs = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_nseg);
   a.plan.capacity = capacity;
+  a.plan.order = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_ord);
   if (direct) a.plan.direct_len = T / N;
   if (want_ckpt) {
     a.plan.ckpt_base = reinterpret_cast<int64_t*>(ws + off_ck);

@@ -73,6 +73,9 @@ struct Plan {
   // > 0: a uniform batch with neither split nor checkpoints, launched without
   // the planner -- segment i is sequence i, direct_len tokens long
   int64_t direct_len = 0;
+  // [capacity], written by the planner: launch rank -> segment id, the
+  // segments in decreasing chunk count (longest first), or null (rank = id)
+  int32_t* order = nullptr;
 };
 
 // Problem description shared by the prefill kernels.

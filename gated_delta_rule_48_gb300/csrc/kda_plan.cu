@@ -104,6 +104,51 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
       *plan.n_segs = s_base;
     }
   }
+
+  // 3. launch order, longest segment first.  The chunk kernels give each SM
+  // the next (segment, head) unit as one frees, so starting the long units
+  // first keeps the short ones (the last segment of each sequence, short
+  // sequences) for the tail.  Counting sort on the chunk count (1024 buckets;
+  // counts above 1023 share the top one), decreasing; the order inside a
+  // bucket is whichever the atomics give, which changes only the schedule,
+  // never a result.
+  if (plan.order == nullptr) return;
+  __syncthreads();
+  if (s_bad) return;
+  const int32_t ns = s_base;
+  int32_t* s_count = s_scan;  // reused: [key]
+  s_count[tid] = 0;
+  __syncthreads();
+  auto key_of = [&](int32_t id) {
+    const int64_t len = plan.segs[id].t1 - plan.segs[id].t0;
+    const int64_t chunks = (len + kChunk - 1) / kChunk;
+    return static_cast<int>(chunks < kPlanThreads - 1 ? chunks : kPlanThreads - 1);
+  };
+  for (int32_t id = tid; id < ns; id += kPlanThreads)
+    if (kda_guard(id, 1, plan.capacity, err)) atomicAdd(&s_count[key_of(id)], 1);
+  __syncthreads();
+  // first rank of key k = number of segments with a larger key: an inclusive
+  // scan in decreasing key order (thread tid holds key kPlanThreads - 1 - tid)
+  const int my_key = kPlanThreads - 1 - tid;
+  const int32_t my_count = s_count[my_key];
+  __syncthreads();
+  s_count[tid] = my_count;  // now indexed by position in decreasing-key order
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int32_t add = tid >= off ? s_count[tid - off] : 0;
+    __syncthreads();
+    s_count[tid] += add;
+    __syncthreads();
+  }
+  const int32_t first = s_count[tid] - my_count;
+  __syncthreads();
+  s_count[my_key] = first;  // back to indexing by key: next free rank of that key
+  __syncthreads();
+  for (int32_t id = tid; id < ns; id += kPlanThreads) {
+    if (!kda_guard(id, 1, plan.capacity, err)) continue;
+    const int32_t rank = atomicAdd(&s_count[key_of(id)], 1);
+    if (kda_guard(rank, 1, plan.capacity, err)) plan.order[rank] = id;
+  }
 }
 
 // Entry states of split sequences, S_in(j+1) = M_j S_in(j) + B_j: one CTA per

@@ -438,8 +438,12 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   // ld.shared / st.shared) instead of falling back to generic accesses
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int32_t seg_id = blockIdx.x;
-  const int h = blockIdx.y;
+  // one block per (segment, head) unit, rank-major: all heads of launch rank
+  // r, then rank r + 1; the planner's order maps ranks to segments, longest
+  // first (the block scheduler hands out blocks in index order)
+  const int32_t rank = static_cast<int32_t>(blockIdx.x / static_cast<uint32_t>(a.H));
+  const int h = static_cast<int>(blockIdx.x % static_cast<uint32_t>(a.H));
+  int32_t seg_id = rank;
   Segment sg;
   if (a.plan.direct_len > 0) {  // uniform batch, no planner: segment = sequence
     if (seg_id >= a.N) return;
@@ -450,7 +454,9 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     sg.count = 1;
     sg.first = seg_id;
   } else {
-    if (seg_id >= *a.plan.n_segs || !kda_guard(seg_id, 1, a.plan.capacity, a.err)) return;
+    if (rank >= *a.plan.n_segs || !kda_guard(rank, 1, a.plan.capacity, a.err)) return;
+    if (a.plan.order) seg_id = a.plan.order[rank];
+    if (!kda_guard(seg_id, 1, a.plan.capacity, a.err)) return;
     sg = a.plan.segs[seg_id];
   }
   const bool last = sg.index + 1 == sg.count;
@@ -1386,7 +1392,9 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.plan.capacity, a.H, 1);
+  const int64_t units = static_cast<int64_t>(a.plan.capacity) * a.H;  // (segment, head) blocks
+  if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<uint32_t>(units), 1, 1);
   prof_begin(s, name);
   prefill_tc_kernel<MODE, FUSED, CKPT, DUMP><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
