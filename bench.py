@@ -116,14 +116,17 @@ def recorded_traffic(kernel, src_file):
     return float(rec["bytes_per_launch"])
 
 
-def recorded_traffic_leg(kernel, workload_idx):
+def recorded_traffic_leg(kernel, workload_idx, segment_tokens=None):
     """DRAM bytes per launch of `kernel` on a long-context workload, from the
-    committed ncu summary, or None (absent, or another version of the source)."""
+    committed ncu summary, or None (absent, another version of the kernel
+    sources, or another segment length than the one this run splits at)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)[f"{kernel}@w{workload_idx}"]
     except (OSError, KeyError, ValueError):
+        return None
+    if "segment_tokens" in rec and rec["segment_tokens"] != segment_tokens:
         return None
     srcs = rec.get("sources", {})
     for f, sha in srcs.items():
@@ -318,7 +321,9 @@ def long_leg(kb, idx, steps, warmup, world, peaks, peak_src):
     # planner reads at most cu_seqlens and writes the segment list (a few KB),
     # so it counts as zero
     traffic = None
-    recs = [0.0 if name == "kda_plan" else recorded_traffic_leg(name, idx) for name in kernels]
+    seg = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H,
+                                     torch.cuda.get_device_properties(0).multi_processor_count)
+    recs = [0.0 if name == "kda_plan" else recorded_traffic_leg(name, idx, seg) for name in kernels]
     if kernels and all(r is not None for r in recs):
         traffic = sum(r * (n / steps) for r, (n, _) in zip(recs, kernels.values()))
     leg = {

@@ -166,8 +166,8 @@ void prof_end(cudaStream_t s, const char* name) {
 // one chunk-time per segment.  Each wave also pays a fixed start (TMEM, the
 // initial state, the first chunk's loads), taken as two chunk-times.  The
 // choice is the s with the least modelled time (sequences taken as T / N
-// tokens each, at least 4 chunks per segment), and no split when splitting
-// does not beat the unsplit time.
+// tokens each, at least 4 chunks per segment, at most 8 replay waves), and no
+// split when splitting does not beat the unsplit time.
 static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count) {
   if (T <= 0 || N <= 0 || H <= 0 || sm_count <= 0) return -1;
   const int64_t chains = static_cast<int64_t>(N) * H, sms = sm_count;
@@ -176,7 +176,9 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
   constexpr int64_t kWaveStart = 2, kMinChunks = 4;
   auto waves = [&](int64_t units) { return (units + sms - 1) / sms; };
   int64_t best = waves(chains) * (len + kWaveStart), best_L = -1;
-  for (int64_t s = 2; s <= len / kMinChunks; ++s) {
+  // beyond 8 waves of replay units every extra segment only adds wave starts
+  const int64_t s_max = std::min(len / kMinChunks, std::max<int64_t>(2, 8 * sms / chains));
+  for (int64_t s = 2; s <= s_max; ++s) {
     const int64_t L = (len + s - 1) / s;     // chunks per segment
     const int64_t segs = (len + L - 1) / L;  // segments per sequence at that length
     if (segs != s) continue;                 // the same cut as a smaller s

@@ -188,10 +188,10 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
  * sequence; split into s segments per sequence, ceil(N H (s - 1) / SMs) summary
  * waves plus ceil(N H s / SMs) replay waves of one segment, plus the scan (one
  * chunk-time per segment) and a fixed start of two chunk-times per wave, with
- * sequences taken as total_tokens / n_seqs tokens and segments of at least
- * 4 chunks.  It returns the length with the least modelled time, or -1 when
- * no split beats the unsplit pass (always when N H >= sm_count).  Invalid
- * sizes (any of them <= 0) return -1.
+ * sequences taken as total_tokens / n_seqs tokens, segments of at least
+ * 4 chunks and at most 8 waves of replay units.  It returns the length with
+ * the least modelled time, or -1 when no split beats the unsplit pass (always
+ * when N H >= sm_count).  Invalid sizes (any of them <= 0) return -1.
  */
 int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
                                 int32_t sm_count);

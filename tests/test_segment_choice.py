@@ -44,6 +44,14 @@ def test_short_sequences_are_not_split(choose):
     assert choose(0, 1, 1, SMS) == -1
 
 
+def test_huge_sequences_choose_quickly(choose):
+    import time
+    t = time.perf_counter()
+    L = choose(1 << 40, 1, 1, SMS)  # 2^34 chunks: the candidate count is bounded
+    assert time.perf_counter() - t < 0.1
+    assert L % 64 == 0 and -(-(1 << 40) // L) <= 8 * SMS
+
+
 def test_invalid_sizes(choose):
     for args in ((-1, 1, 1, SMS), (4096, 0, 1, SMS), (4096, 1, 0, SMS), (4096, 1, 1, 0)):
         assert choose(*args) == -1
@@ -67,5 +75,6 @@ def test_choice_minimises_the_documented_model(choose, T, N, H, sms):
     L = choose(T, N, H, sms)
     got = modelled(T, N, H, sms, None if L == -1 else L // 64)
     n = -(-(-(-T // N)) // 64)
-    others = [modelled(T, N, H, sms, c) for c in range(4, n) if -(-n // c) >= 2]
+    cap = max(2, 8 * sms // (N * H))  # at most 8 waves of replay units
+    others = [modelled(T, N, H, sms, c) for c in range(4, n) if 2 <= -(-n // c) <= cap]
     assert got <= min(others + [modelled(T, N, H, sms, None)])
