@@ -114,6 +114,26 @@ def test_segment_split_matches_oracle(seg, la):
             segment_tokens=seg)
 
 
+def test_automatic_split_is_the_documented_length():
+    """kda_chunk_fwd's automatic split is an explicit split at the length
+    kda_auto_segment_tokens reports for this device: the same launches, so
+    bit-identical results."""
+    p = kin.make_prefill([3000, 1700], 2, 128, seed=38, s0_std=0.05, log_alpha_fixed=-0.02)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H, sms)
+    assert L > 0  # 4 chains on this part: the model splits
+    d = to_device(p)
+    auto = kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
+                            d["cu_seqlens"], n_seqs=p.n_seqs, segment_tokens=0)
+    expl = kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
+                            d["cu_seqlens"], n_seqs=p.n_seqs, segment_tokens=L)
+    assert kb.kda_get_device_error() == 0
+    assert torch.equal(auto[0], expl[0]) and torch.equal(auto[1], expl[1])
+    ref_o, ref_S = oracle_prefill(p)
+    check_out(auto[0].float().cpu().numpy(), ref_o)
+    check_state(auto[1].cpu().numpy(), ref_S)
+
+
 def test_segment_split_d64_and_no_split_agree():
     p = kin.make_prefill([999, 257], 2, 64, seed=36, s0_std=0.05, log_alpha_fixed=-0.03)
     o1, S1 = compare(p, segment_tokens=128)
