@@ -134,6 +134,17 @@ def test_automatic_split_is_the_documented_length():
     check_state(auto[1].cpu().numpy(), ref_S)
 
 
+@pytest.mark.parametrize("seg", [0, 64])
+def test_thousands_of_sequences(seg):
+    """2,500 packed sequences of 0..199 tokens: the planner walks them in
+    blocks of 1,024, and with 64-token segments it emits and orders some 5,000
+    segments (several per chunk-count bucket)."""
+    rng = np.random.default_rng(44)
+    lens = [int(x) for x in rng.integers(0, 200, size=2500)]
+    compare(kin.make_prefill(lens, 2, 64, seed=44, s0_std=0.05, log_alpha_fixed=-0.05),
+            segment_tokens=seg)
+
+
 def test_segment_split_d64_and_no_split_agree():
     p = kin.make_prefill([999, 257], 2, 64, seed=36, s0_std=0.05, log_alpha_fixed=-0.03)
     o1, S1 = compare(p, segment_tokens=128)
