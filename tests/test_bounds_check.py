@@ -53,6 +53,8 @@ CHILD_TESTS = [
     "tests/test_parity.py::test_varlen_short_and_long_with_empty",
     "tests/test_parity.py::test_segment_split_matches_oracle",
     "tests/test_parity.py::test_segment_split_d64_and_no_split_agree",
+    "tests/test_parity.py::test_automatic_split_is_the_documented_length",
+    "tests/test_parity.py::test_thousands_of_sequences",
     "tests/test_parity.py::test_state_aliasing_continuation",
     "tests/test_parity.py::test_decode_steps_equal_prefill_of_same_tokens",
     "tests/test_parity.py::test_empty_sequences_hand_state_through",
