@@ -322,7 +322,8 @@ def long_leg(kb, idx, steps, warmup, world, peaks, peak_src):
     # so it counts as zero
     traffic = None
     seg = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H,
-                                     torch.cuda.get_device_properties(0).multi_processor_count)
+                                     torch.cuda.get_device_properties(0).multi_processor_count,
+                                     p.uniform)
     recs = [0.0 if name == "kda_plan" else recorded_traffic_leg(name, idx, seg) for name in kernels]
     if kernels and all(r is not None for r in recs):
         traffic = sum(r * (n / steps) for r, (n, _) in zip(recs, kernels.values()))

@@ -176,7 +176,7 @@ def load():
             lib.kda_workspace_pool_bytes.argtypes = []
             lib.kda_auto_segment_tokens.restype = ctypes.c_int64
             lib.kda_auto_segment_tokens.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
-                                                    ctypes.c_int32]
+                                                    ctypes.c_int32, ctypes.c_int32]
             lib.kda_selftest_bounded_wait.restype = ctypes.c_int
             lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
             lib.kda_selftest_bounds_check.restype = ctypes.c_int
@@ -366,9 +366,11 @@ def kda_debug_chunk_dump(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, 
     return out, S_final, parts
 
 
-def kda_auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count) -> int:
-    """The segment length the automatic split picks (-1: no split); host only."""
-    return int(load().kda_auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count))
+def kda_auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count, uniform) -> int:
+    """The segment length the automatic split picks (-1: no split); host only.
+    ``uniform``: the batch has cu_seqlens None (sequences of equal length)."""
+    return int(load().kda_auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count,
+                                              1 if uniform else 0))
 
 
 def kda_workspace_pool_bytes() -> int:

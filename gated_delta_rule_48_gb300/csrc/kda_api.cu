@@ -161,14 +161,24 @@ void prof_end(cudaStream_t s, const char* name) {
 // fixed time per 64-token chunk, one CTA per SM, so a pass over U units of at
 // most L chunks takes about ceil(U / SMs) waves of L chunk-times.  Unsplit, the
 // N H chains take ceil(N H / SMs) waves of the whole sequence.  Split into s
-// segments per sequence, the summary pass runs the N H (s - 1) non-final units
-// and the replay all N H s units, and the scan of the entry states adds about
-// one chunk-time per segment.  Each wave also pays a fixed start (TMEM, the
-// initial state, the first chunk's loads), taken as two chunk-times.  The
-// choice is the s with the least modelled time (sequences taken as T / N
-// tokens each, at least 4 chunks per segment, at most 8 replay waves), and no
-// split when splitting does not beat the unsplit time.
-static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count) {
+// segments per sequence, a uniform batch's first pass runs N H (s - 1) units
+// (the replays of segment 0 and the summaries of segments 1 .. s - 2) and its
+// second pass the N H (s - 1) replays of segments 1 .. s - 1; the scan of the
+// entry states adds about one chunk-time per segment.  Each wave also pays a fixed start
+// (TMEM, the initial state, the first chunk's loads), taken as two
+// chunk-times.  The choice is the s with the least modelled time (at least 4
+// chunks per segment, at most 8 replay waves), and no split when splitting
+// does not beat the unsplit time.
+//
+// The model takes every sequence as T / N tokens long, which is exact for a
+// uniform batch.  A packed batch's lengths live on the device; there the
+// first pass only summarises (N H (s - 1) units) and the second replays every
+// segment (N H s units), the model counts exactly that, and its shorter
+// segments keep both passes balanced when the lengths are very uneven.  (On
+// log-uniform length mixes of 1,048,576 tokens, a list-scheduling simulation
+// puts that choice within ~3 % of the best fixed length; replaying segment 0
+// in the first pass at the uniform count's length lost up to 20 % there.)
+static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count, bool uniform) {
   if (T <= 0 || N <= 0 || H <= 0 || sm_count <= 0) return -1;
   const int64_t chains = static_cast<int64_t>(N) * H, sms = sm_count;
   if (chains >= sms) return -1;
@@ -182,7 +192,9 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
     const int64_t L = (len + s - 1) / s;     // chunks per segment
     const int64_t segs = (len + L - 1) / L;  // segments per sequence at that length
     if (segs != s) continue;                 // the same cut as a smaller s
-    const int64_t t = (waves(chains * (segs - 1)) + waves(chains * segs)) * (L + kWaveStart) + segs;
+    const int64_t second = uniform ? segs - 1 : segs;
+    const int64_t t =
+        (waves(chains * (segs - 1)) + waves(chains * second)) * (L + kWaveStart) + segs;
     if (t < best) {
       best = t;
       best_L = L;
@@ -192,8 +204,8 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
 }
 
 extern "C" int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
-                                           int32_t sm_count) {
-  return auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count);
+                                           int32_t sm_count, int32_t uniform) {
+  return auto_segment_tokens(total_tokens, n_seqs, n_heads, sm_count, uniform != 0);
 }
 
 // Host-side checks of a prefill call; nothing is launched unless all pass.
@@ -289,7 +301,7 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   cudaStream_t s = static_cast<cudaStream_t>(stream_v);
 
   int64_t L = segment_tokens;
-  if (L == 0) L = auto_segment_tokens(T, N, H, dev->sm_count);
+  if (L == 0) L = auto_segment_tokens(T, N, H, dev->sm_count, cu_seqlens == nullptr);
   bool split = L > 0 && L < T;
   if (!split) L = -1;
   const int64_t capacity64 = split ? static_cast<int64_t>(N) + (T + L - 1) / L + 1 : N;
@@ -311,8 +323,11 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   const bool want_ckpt = ckpt_interval > 0;  // the planner counts (and flags an overflow) even if max = 0
   size_t off_ck = align_up(off_es + es_bytes);
   size_t ck_base_bytes = want_ckpt ? sizeof(int64_t) * (size_t)N : 0;
-  size_t off_ord = align_up(off_ck + ck_base_bytes);  // launch order, longest segment first
-  size_t ws_bytes = align_up(off_ord + sizeof(int32_t) * capacity);
+  // launch orders, longest segment first: the first pass's, the second pass's, their lengths
+  size_t off_ord = align_up(off_ck + ck_base_bytes);
+  size_t off_ord2 = align_up(off_ord + sizeof(int32_t) * capacity);
+  size_t off_nord = align_up(off_ord2 + sizeof(int32_t) * capacity);
+  size_t ws_bytes = align_up(off_nord + 2 * sizeof(int32_t));
 
   // A uniform batch with neither split nor checkpoints needs no plan and no
   // workspace: the chunk kernel takes segment i = sequence i.
@@ -351,6 +366,9 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.plan.n_segs = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_nseg);
   a.plan.capacity = capacity;
   a.plan.order = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_ord);
+  a.plan.order2 = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_ord2);
+  a.plan.n_order = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_nord);
+  a.plan.first_replayed = split && cu_seqlens == nullptr ? 1 : 0;  // uniform batches
   if (direct) a.plan.direct_len = T / N;
   if (want_ckpt) {
     a.plan.ckpt_base = reinterpret_cast<int64_t*>(ws + off_ck);
@@ -366,9 +384,14 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
 
   kda_status result = KDA_OK;
   if (!direct) e = launch_plan(cu_seqlens, T, N, L, a.plan, a.err, s);
-  if (e == cudaSuccess && split) e = launch_prefill_summary(a, s);
-  if (e == cudaSuccess && split) e = launch_segment_scan(a, s);
-  if (e == cudaSuccess) e = dump ? launch_prefill_replay_dump(a, s) : launch_prefill_replay(a, s);
+  if (split) {  // summaries (and, uniform, first segments replayed); scan; replays
+    if (e == cudaSuccess) e = launch_prefill_pass1(a, s);
+    if (e == cudaSuccess) e = launch_segment_scan(a, s);
+    a.pass = 2;
+    if (e == cudaSuccess) e = launch_prefill_replay(a, s);
+  } else if (e == cudaSuccess) {
+    e = dump ? launch_prefill_replay_dump(a, s) : launch_prefill_replay(a, s);
+  }
   if (e != cudaSuccess) result = cuda_fail(e, "prefill launch");
   if (ws) {
     cudaError_t ef = cudaFreeAsync(ws, s);

@@ -73,9 +73,21 @@ struct Plan {
   // > 0: a uniform batch with neither split nor checkpoints, launched without
   // the planner -- segment i is sequence i, direct_len tokens long
   int64_t direct_len = 0;
-  // [capacity], written by the planner: launch rank -> segment id, the
-  // segments in decreasing chunk count (longest first), or null (rank = id)
+  // Launch orders written by the planner, each longest first (decreasing
+  // chunk count): order [capacity] for the first pass, order2 [capacity] for
+  // the second pass of a split prefill, n_order [2] their lengths; order null:
+  // rank = segment id.  Unsplit: order lists every segment.  Split with
+  // first_replayed: order = every segment but the last one of a split
+  // sequence, order2 = the segments with index >= 1.  Split otherwise: order =
+  // every segment but the last one of its sequence, order2 = every segment.
+  // (A sequence shorter than the segment length is one segment, its last.)
   int32_t* order = nullptr;
+  int32_t* order2 = nullptr;
+  int32_t* n_order = nullptr;
+  // split prefills: 1 when the first pass replays segment 0 of every sequence
+  // (uniform batches), 0 when it only summarises (every segment but the last)
+  // and the second pass replays all segments (packed batches)
+  int32_t first_replayed = 0;
 };
 
 // Problem description shared by the prefill kernels.
@@ -106,6 +118,7 @@ struct PrefillArgs {
   float* dump = nullptr;
   int32_t dump_seg = -1, dump_head = -1;
   int64_t dump_chunk = -1;
+  int pass = 1;  // which launch order the kernels walk (2: a split prefill's second pass)
 };
 
 // Layout of the intermediate dump, in floats: g [64][128], A_kk [64][64],
@@ -150,9 +163,11 @@ cudaError_t launch_plan(const int32_t* cu_seqlens, int64_t T, int32_t N,
 cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 
 // ---- chunked prefill (kda_prefill_*.cu)
-// pass 0: summary (B_j, M_j) of every non-final segment; pass 1: replay.
-// tcgen05 kernels (kda_prefill_tc.cu), dk = dv = 128 or 64
-cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s);
+// tcgen05 kernels (kda_prefill_tc.cu), dk = dv = 128 or 64.  Split prefill:
+// pass 1 replays the first segment of every sequence (from S0) and summarises
+// (B_j, M_j) the middle ones, in one launch; the scan chains the entry states;
+// pass 2 (a.pass = 2) replays segments 1 .. count - 1.  Unsplit: one replay.
+cudaError_t launch_prefill_pass1(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
 // the replay with the intermediate dump of a.dump (one chunk of one unit)
 cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s);

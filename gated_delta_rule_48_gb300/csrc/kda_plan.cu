@@ -10,10 +10,12 @@
 // "Parallelizing Sequential State Updates"; orkas.ai close read, section "The
 // bill comes due in the serving stack"): a segment maps its entry state
 // affinely, S_end = M S_in + B, where B is the segment run from a zero state
-// and M the segment's transition.  The summary pass computes (B_j, M_j) of
+// and M the segment's transition.  The first pass computes (B_j, M_j) of
 // every segment but each sequence's last; the scan below chains them,
-// S_in(j+1) = M_j S_in(j) + B_j, and the replay pass restarts each segment
-// from its exact entry state.
+// S_in(j+1) = M_j S_in(j) + B_j, and the second pass replays every segment
+// from its exact entry state.  In a uniform batch the first pass replays
+// segment 0 instead of summarising it (its exit state is S_in(1)), so the
+// second pass replays segments 1 .. count - 1 only.
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -34,7 +36,10 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
   __shared__ int64_t s_cbase;
   const int tid = threadIdx.x;
   const int64_t CI = plan.ckpt_interval;
-  if (tid == 0) { s_bad = 0; s_base = 0; s_cbase = 0; }
+  if (tid == 0) {
+    s_bad = 0; s_base = 0; s_cbase = 0;
+    if (plan.n_order) plan.n_order[0] = plan.n_order[1] = 0;  // no units unless the plan completes
+  }
   __syncthreads();
 
   // 1. validate cu_seqlens
@@ -105,53 +110,67 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
     }
   }
 
-  // 3. launch order, longest segment first.  The chunk kernels give each SM
+  // 3. launch orders, longest segment first.  The chunk kernels give each SM
   // the next (segment, head) unit as one frees, so starting the long units
   // first keeps the short ones (the last segment of each sequence, short
   // sequences) for the tail.  Counting sort on the chunk count (1024 buckets;
   // counts above 1023 share the top one), decreasing; the order inside a
   // bucket is whichever the atomics give, which changes only the schedule,
-  // never a result.
+  // never a result.  The lists are those of Plan::order and Plan::order2
+  // (kda_internal.h); unsplit, list 0 holds every segment.
   if (plan.order == nullptr) return;
   __syncthreads();
   if (s_bad) return;
   const int32_t ns = s_base;
   int32_t* s_count = s_scan;  // reused: [key]
-  s_count[tid] = 0;
-  __syncthreads();
   auto key_of = [&](int32_t id) {
     const int64_t len = plan.segs[id].t1 - plan.segs[id].t0;
     const int64_t chunks = (len + kChunk - 1) / kChunk;
     return static_cast<int>(chunks < kPlanThreads - 1 ? chunks : kPlanThreads - 1);
   };
-  for (int32_t id = tid; id < ns; id += kPlanThreads)
-    if (kda_guard(id, 1, plan.capacity, err)) atomicAdd(&s_count[key_of(id)], 1);
-  __syncthreads();
-  // first rank of key k = number of segments with a larger key: an inclusive
-  // scan in decreasing key order (thread tid holds key kPlanThreads - 1 - tid)
-  const int my_key = kPlanThreads - 1 - tid;
-  const int32_t my_count = s_count[my_key];
-  __syncthreads();
-  s_count[tid] = my_count;  // now indexed by position in decreasing-key order
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int32_t add = tid >= off ? s_count[tid - off] : 0;
+  for (int list = 0; list < 2; ++list) {
+    int32_t* out = list ? plan.order2 : plan.order;
+    auto in_list = [&](int32_t id) {
+      const Segment& g = plan.segs[id];
+      if (L <= 0) return list == 0;  // unsplit: one pass over every segment
+      if (plan.first_replayed) return list ? g.index >= 1 : (g.index == 0 || g.index + 1 < g.count);
+      return list ? true : g.index + 1 < g.count;
+    };
+    s_count[tid] = 0;
     __syncthreads();
-    s_count[tid] += add;
+    for (int32_t id = tid; id < ns; id += kPlanThreads)
+      if (kda_guard(id, 1, plan.capacity, err) && in_list(id)) atomicAdd(&s_count[key_of(id)], 1);
     __syncthreads();
-  }
-  const int32_t first = s_count[tid] - my_count;
-  __syncthreads();
-  s_count[my_key] = first;  // back to indexing by key: next free rank of that key
-  __syncthreads();
-  for (int32_t id = tid; id < ns; id += kPlanThreads) {
-    if (!kda_guard(id, 1, plan.capacity, err)) continue;
-    const int32_t rank = atomicAdd(&s_count[key_of(id)], 1);
-    if (kda_guard(rank, 1, plan.capacity, err)) plan.order[rank] = id;
+    // first rank of key k = number of listed segments with a larger key: an
+    // inclusive scan in decreasing key order (thread tid holds key
+    // kPlanThreads - 1 - tid)
+    const int my_key = kPlanThreads - 1 - tid;
+    const int32_t my_count = s_count[my_key];
+    __syncthreads();
+    s_count[tid] = my_count;  // now indexed by position in decreasing-key order
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {
+      const int32_t add = tid >= off ? s_count[tid - off] : 0;
+      __syncthreads();
+      s_count[tid] += add;
+      __syncthreads();
+    }
+    const int32_t first = s_count[tid] - my_count;
+    if (tid == kPlanThreads - 1) plan.n_order[list] = s_count[tid];  // the list's length
+    __syncthreads();
+    s_count[my_key] = first;  // back to indexing by key: next free rank of that key
+    __syncthreads();
+    for (int32_t id = tid; id < ns; id += kPlanThreads) {
+      if (!kda_guard(id, 1, plan.capacity, err) || !in_list(id)) continue;
+      const int32_t rank = atomicAdd(&s_count[key_of(id)], 1);
+      if (kda_guard(rank, 1, plan.capacity, err)) out[rank] = id;
+    }
+    __syncthreads();  // s_count is reused by the next list
   }
 }
 
-// Entry states of split sequences, S_in(j+1) = M_j S_in(j) + B_j: one CTA per
+// Entry states of split sequences, S_in(j+1) = M_j S_in(j) + B_j, from S0 or,
+// when the first pass replayed segment 0, from the S_in(1) it wrote: one CTA per
 // (sequence, head, block of kScanCols state columns), sequential over the
 // sequence's segments.  The whole M_j (D x D f32, from the summary records)
 // is staged in shared memory by cp.async, the next segment's copy in flight
@@ -204,7 +223,11 @@ segment_scan_kernel(PrefillArgs a) {
     }
   }
   __syncthreads();
-  if (s_first < 0 || s_count <= 1) return;
+  // first_replayed: segment 0 was replayed in the first pass, which wrote
+  // S_in(1); the chain starts there, so sequences of 2 segments need nothing
+  // here.  Otherwise the chain starts from S0 with segment 0's record.
+  const int j0 = a.plan.first_replayed ? 1 : 0;  // first segment chained here
+  if (s_first < 0 || s_count <= 1 + j0) return;
   // records and entry states are D (128) wide; the caller's S0 is a.dv wide
   // (64 runs zero-padded to 128)
   const int W = 2 * D;  // width of the B | M record
@@ -222,17 +245,23 @@ segment_scan_kernel(PrefillArgs a) {
     }
     cp_async_commit();
   };
-  stage_M(0, rec_off(s_first));
-  for (int i = tid; i < D * kScanCols; i += kScanThreads) {
+  stage_M(0, rec_off(s_first + j0));
+  for (int i = tid; i < D * kScanCols; i += kScanThreads) {  // S_in(j0)
     const int c = i / kScanCols, j = i % kScanCols;
-    const int64_t e = ((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j;
-    sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO &&
-               kda_guard(e, 1, static_cast<int64_t>(a.N) * a.H * DIO * DIO, a.err))
-                  ? a.S0[e]
-                  : 0.f;
+    if (j0) {
+      const int64_t e = ((static_cast<int64_t>(s_first) + 1) * a.H + h) * static_cast<int64_t>(D) * D +
+                        static_cast<int64_t>(c) * D + col0 + j;
+      sm.S[i] = kda_guard(e, 1, n_es, a.err) ? a.entry_state[e] : 0.f;
+    } else {
+      const int64_t e = ((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j;
+      sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO &&
+                 kda_guard(e, 1, static_cast<int64_t>(a.N) * a.H * DIO * DIO, a.err))
+                    ? a.S0[e]
+                    : 0.f;
+    }
   }
   const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + 32 r
-  for (int sgi = 0; sgi + 1 < s_count; ++sgi) {
+  for (int sgi = j0; sgi + 1 < s_count; ++sgi) {
     const int64_t seg = s_first + sgi;
     const int64_t roff = rec_off(seg);
     float acc[RPT];
@@ -242,13 +271,13 @@ segment_scan_kernel(PrefillArgs a) {
       acc[r] = kda_guard(e, 1, n_it, a.err) ? a.incr_trans[e] : 0.f;
     }
     if (sgi + 2 < s_count) {  // stage the next transition while this one is used
-      stage_M((sgi + 1) & 1, rec_off(seg + 1));
+      stage_M((sgi - j0 + 1) & 1, rec_off(seg + 1));
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const float* Mb = sm.M[sgi & 1];
+    const float* Mb = sm.M[(sgi - j0) & 1];
 #pragma unroll 4
     for (int m = 0; m < D; ++m) {
       const float sv = sm.S[m * kScanCols + j];

@@ -425,40 +425,45 @@ __device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, in
   }
 }
 
-// CKPT (replay only): write the state checkpoints the plan asks for; a separate
-// instantiation, so the plain replay keeps its register budget.
-// DUMP (replay only): also write the intermediates of one chunk of one unit
-// (a.dump); a separate instantiation with extra barriers, for debugging.
-template <int MODE, bool FUSED, bool CKPT, bool DUMP = false>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  // 1024-byte aligned base, derived from the shared array by an offset so the
-  // compiler keeps every access in the shared window (32-bit addressing,
-  // ld.shared / st.shared) instead of falling back to generic accesses
-  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // one block per (segment, head) unit, rank-major: all heads of launch rank
-  // r, then rank r + 1; the planner's order maps ranks to segments, longest
-  // first (the block scheduler hands out blocks in index order)
+// The (segment, head) unit of this block: one block per unit, rank-major (all
+// heads of launch rank r, then rank r + 1).  The planner's order maps ranks
+// to segments, longest first (the block scheduler hands out blocks in index
+// order); pass 2 of a split prefill takes its own list.  False: no unit.
+__device__ __forceinline__ bool unit_of(const PrefillArgs& a, int32_t& seg_id, Segment& sg,
+                                        int& h) {
   const int32_t rank = static_cast<int32_t>(blockIdx.x / static_cast<uint32_t>(a.H));
-  const int h = static_cast<int>(blockIdx.x % static_cast<uint32_t>(a.H));
-  int32_t seg_id = rank;
-  Segment sg;
+  h = static_cast<int>(blockIdx.x % static_cast<uint32_t>(a.H));
+  seg_id = rank;
   if (a.plan.direct_len > 0) {  // uniform batch, no planner: segment = sequence
-    if (seg_id >= a.N) return;
+    if (seg_id >= a.N) return false;
     sg.t0 = static_cast<int64_t>(seg_id) * a.plan.direct_len;
     sg.t1 = sg.t0 + a.plan.direct_len;
     sg.seq = seg_id;
     sg.index = 0;
     sg.count = 1;
     sg.first = seg_id;
-  } else {
-    if (rank >= *a.plan.n_segs || !kda_guard(rank, 1, a.plan.capacity, a.err)) return;
-    if (a.plan.order) seg_id = a.plan.order[rank];
-    if (!kda_guard(seg_id, 1, a.plan.capacity, a.err)) return;
-    sg = a.plan.segs[seg_id];
+    return true;
   }
+  const int32_t* ord = a.pass == 2 ? a.plan.order2 : a.plan.order;
+  const int32_t count = ord ? a.plan.n_order[a.pass == 2 ? 1 : 0] : *a.plan.n_segs;
+  if (rank >= count || !kda_guard(rank, 1, a.plan.capacity, a.err)) return false;
+  if (ord) seg_id = ord[rank];
+  if (!kda_guard(seg_id, 1, a.plan.capacity, a.err)) return false;
+  sg = a.plan.segs[seg_id];
+  return true;
+}
+
+// One (segment, head) unit, in summary or replay mode (see the file header).
+template <int MODE, bool FUSED, bool CKPT, bool DUMP>
+__device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const PrefillArgs& a,
+                                                const int32_t seg_id, const Segment& sg,
+                                                const int h) {
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte aligned base, derived from the shared array by an offset so the
+  // compiler keeps every access in the shared window (32-bit addressing,
+  // ld.shared / st.shared) instead of falling back to generic accesses
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool last = sg.index + 1 == sg.count;
   if (MODE == kModeSummary && last) return;
   // A summary unit carries two states through the segment: the increment B
@@ -1309,6 +1314,10 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
         if (last && a.S_final)
           store_state(a.S_final, (static_cast<int64_t>(sg.seq) * H + h) * DIO * DIO,
                       static_cast<int64_t>(a.N) * H * DIO * DIO, DIO, kColS, DIO);
+        else if (a.plan.first_replayed && !last && sg.index == 0 && a.entry_state)
+          // the first pass's replay of segment 0: the entry state of segment 1
+          store_state(a.entry_state, (static_cast<int64_t>(seg_id + 1) * H + h) * D * D,
+                      static_cast<int64_t>(a.plan.capacity) * H * D * D, D, kColS, D);
       } else {  // the increment | transition record, rows of 2 D floats
         const int64_t off = (static_cast<int64_t>(seg_id) * H + h) * D * (2 * D);
         const int64_t n_it = static_cast<int64_t>(a.plan.capacity) * H * D * (2 * D);
@@ -1321,6 +1330,37 @@ prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
   __syncthreads();
   tc_fence_after();
   if (warp == kWarps) tmem_dealloc(tmem, kTmemCols);
+}
+
+// CKPT (replay only): write the state checkpoints the plan asks for; a separate
+// instantiation, so the plain replay keeps its register budget.
+// DUMP (replay only): also write the intermediates of one chunk of one unit
+// (a.dump); a separate instantiation with extra barriers, for debugging.
+template <int MODE, bool FUSED, bool CKPT, bool DUMP = false>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
+  int32_t seg_id;
+  Segment sg;
+  int h;
+  if (!unit_of(a, seg_id, sg, h)) return;
+  prefill_tc_body<MODE, FUSED, CKPT, DUMP>(maps, a, seg_id, sg, h);
+}
+
+// First pass of a split prefill, one launch: every segment but the last one
+// of its sequence is summarised, except that with first_replayed (uniform
+// batches) the first segment of every sequence is replayed from S0 instead,
+// writing its outputs and the entry state of segment 1.
+template <bool FUSED, bool CKPT>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_pass1_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
+  int32_t seg_id;
+  Segment sg;
+  int h;
+  if (!unit_of(a, seg_id, sg, h)) return;
+  if (a.plan.first_replayed && sg.index == 0)
+    prefill_tc_body<kModeReplay, FUSED, CKPT, false>(maps, a, seg_id, sg, h);
+  else
+    prefill_tc_body<kModeSummary, FUSED, false, false>(maps, a, seg_id, sg, h);
 }
 
 // ---- host side: TMA descriptors
@@ -1361,8 +1401,19 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool FUSED, bool CKPT, bool DUMP = false>
+// The kernel a launch runs: one mode, or (PASS1) the mixed first pass.
+template <int MODE, bool FUSED, bool CKPT, bool DUMP, bool PASS1>
+struct KernelOf {
+  static constexpr auto fn = prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>;
+};
+template <int MODE, bool FUSED, bool CKPT, bool DUMP>
+struct KernelOf<MODE, FUSED, CKPT, DUMP, true> {
+  static constexpr auto fn = prefill_pass1_kernel<FUSED, CKPT>;
+};
+
+template <int MODE, bool FUSED, bool CKPT, bool DUMP = false, bool PASS1 = false>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
+  constexpr auto kern = KernelOf<MODE, FUSED, CKPT, DUMP, PASS1>::fn;
   if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
   memset(&maps, 0, sizeof maps);
@@ -1383,29 +1434,31 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
   static int launch_regs = -1;
   if (launch_regs < 0) {
     cudaFuncAttributes fa;
-    const cudaError_t ea = cudaFuncGetAttributes(&fa, prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>);
+    const cudaError_t ea = cudaFuncGetAttributes(&fa, kern);
     if (ea != cudaSuccess) return ea;
     launch_regs = fa.numRegs;
   }
   if (static_cast<uint32_t>(launch_regs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int64_t units = static_cast<int64_t>(a.plan.capacity) * a.H;  // (segment, head) blocks
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   dim3 grid(static_cast<uint32_t>(units), 1, 1);
   prof_begin(s, name);
-  prefill_tc_kernel<MODE, FUSED, CKPT, DUMP><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(maps, a);
   prof_end(s, name);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_summary(const PrefillArgs& a, cudaStream_t s) {
-  return a.fused ? launch_tc<kModeSummary, true, false>(a, s, "kda_prefill_summary")
-                 : launch_tc<kModeSummary, false, false>(a, s, "kda_prefill_summary");
+cudaError_t launch_prefill_pass1(const PrefillArgs& a, cudaStream_t s) {
+  if (a.ckpt)
+    return a.fused ? launch_tc<kModeReplay, true, true, false, true>(a, s, "kda_prefill_pass1")
+                   : launch_tc<kModeReplay, false, true, false, true>(a, s, "kda_prefill_pass1");
+  return a.fused ? launch_tc<kModeReplay, true, false, false, true>(a, s, "kda_prefill_pass1")
+                 : launch_tc<kModeReplay, false, false, false, true>(a, s, "kda_prefill_pass1");
 }
 
 cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s) {

@@ -103,7 +103,7 @@ typedef enum {
  * Memory: a uniform batch (cu_seqlens = NULL) whose sequences are not split
  * allocates nothing and is one kernel launch.  Otherwise the call allocates a
  * temporary workspace stream-ordered on `stream` and frees it there: the
- * segment plan (32 bytes per segment) and, when sequences are split,
+ * segment plan (40 bytes per segment) and, when sequences are split,
  * (N + T / segment) * H * dk * (2 dv + dk) * 4 bytes of segment summaries and
  * entry states.
  */
@@ -164,10 +164,13 @@ kda_status kda_decode_step_t(const kda_tensor *q, const kda_tensor *k,
  *
  * segment_tokens = 0 chooses automatically (what kda_chunk_fwd does).
  * segment_tokens > 0 must be a multiple of 64: every sequence longer than it
- * is cut into segments of that many tokens (the last may be shorter), each
- * segment's zero-start increment B and transition M are computed in
- * parallel, the entry states S_in(j+1) = M_j S_in(j) + B_j are scanned, and
- * the segments are replayed from their entry states.  segment_tokens < 0
+ * is cut into segments of that many tokens (the last may be shorter).  A
+ * first launch computes the zero-start increment B and the transition M of
+ * every segment but each sequence's last, the entry states S_in(j+1) =
+ * M_j S_in(j) + B_j are scanned, and a second launch replays every segment
+ * from its entry state.  In a uniform batch (cu_seqlens NULL) the first launch
+ * replays segment 0 from S0 instead of summarising it (its exit state is
+ * S_in(1)), so the second replays segments 1 .. last only.  segment_tokens < 0
  * disables splitting.  The result is the same up to rounding; this is the
  * scheduling knob behind the automatic choice.
  */
@@ -182,19 +185,26 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
  * kda_auto_segment_tokens -- the segment length segment_tokens = 0 chooses.
  *
  * Host only: touches no device.  sm_count is the device's multiprocessor
- * count (kda_chunk_fwd uses the current device's).  Returns a multiple of 64,
- * or -1 for no split.  The choice models each chunk kernel pass as waves of
- * one (segment, head) unit per SM: unsplit, ceil(N H / SMs) waves of the whole
- * sequence; split into s segments per sequence, ceil(N H (s - 1) / SMs) summary
- * waves plus ceil(N H s / SMs) replay waves of one segment, plus the scan (one
- * chunk-time per segment) and a fixed start of two chunk-times per wave, with
- * sequences taken as total_tokens / n_seqs tokens, segments of at least
- * 4 chunks and at most 8 waves of replay units.  It returns the length with
- * the least modelled time, or -1 when no split beats the unsplit pass (always
- * when N H >= sm_count).  Invalid sizes (any of them <= 0) return -1.
+ * count (kda_chunk_fwd uses the current device's); uniform is 1 for a uniform
+ * batch (cu_seqlens NULL), 0 for a packed one.  Returns a multiple of 64, or
+ * -1 for no split.  The choice models each chunk kernel pass as waves of one
+ * (segment, head) unit per SM: unsplit, ceil(N H / SMs) waves of the whole
+ * sequence; split into s segments per sequence, a first pass of
+ * ceil(N H (s - 1) / SMs) waves of one segment and a second of
+ * ceil(N H (s - 1) / SMs) waves for a uniform batch (replays of segment 0 and
+ * summaries of segments 1 .. s - 2, then replays of segments 1 .. s - 1), of
+ * ceil(N H s / SMs) waves for a packed one (summaries of segments 0 .. s - 2,
+ * then replays of every segment: shorter segments, which balance the uneven
+ * lengths that only the device reads).
+ * Plus the scan (one chunk-time per segment) and a fixed start of two
+ * chunk-times per wave, with sequences taken as total_tokens / n_seqs tokens,
+ * segments of at least 4 chunks and at most 8 waves of replay units.  It
+ * returns the length with the least modelled time, or -1 when no split beats
+ * the unsplit pass (always when N H >= sm_count).  Invalid sizes (any of them
+ * <= 0) return -1.
  */
 int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
-                                int32_t sm_count);
+                                int32_t sm_count, int32_t uniform);
 
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd without any device allocation.

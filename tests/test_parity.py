@@ -120,7 +120,7 @@ def test_automatic_split_is_the_documented_length():
     bit-identical results."""
     p = kin.make_prefill([3000, 1700], 2, 128, seed=38, s0_std=0.05, log_alpha_fixed=-0.02)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    L = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H, sms)
+    L = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H, sms, False)  # packed
     assert L > 0  # 4 chains on this part: the model splits
     d = to_device(p)
     auto = kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],

@@ -1,6 +1,7 @@
 """The automatic segment length of the split prefill (kda_auto_segment_tokens,
 host only): no split when the (sequence, head) chains fill the GPU, the
-wave-filling lengths on the long-context shapes, and the documented limits."""
+wave-filling lengths on the long-context shapes (uniform and packed batches),
+and the documented limits."""
 import pytest
 
 from gated_delta_rule_48_gb300 import binding as kb
@@ -11,7 +12,7 @@ SMS = 152
 @pytest.fixture(scope="module")
 def choose():
     kb.build()
-    return kb.kda_auto_segment_tokens
+    return lambda T, N, H, sms, uniform=True: kb.kda_auto_segment_tokens(T, N, H, sms, uniform)
 
 
 def test_enough_chains_means_no_split(choose):
@@ -21,13 +22,15 @@ def test_enough_chains_means_no_split(choose):
 
 
 def test_long_context_shapes(choose):
-    # 1 x 65,536 tokens, H16: 9 segments of 114 chunks -> 128 summary units and
-    # 144 replay units, one wave each
-    assert choose(65536, 1, 16, SMS) == 114 * 64
-    # 8 x 131,072 tokens, H8: 7 segments of 293 chunks -> 384 summary and 448
-    # replay units, three waves each (four segments of 547 chunks would take
-    # two waves of 547 in each pass: 2188 against 1758 chunk-times)
-    assert choose(8 * 131072, 8, 8, SMS) == 293 * 64
+    # uniform 1 x 65,536 tokens, H16: 10 segments of 103 chunks -> 144 units in
+    # each pass (16 replays of segment 0 + 128 summaries, then 144 replays),
+    # one wave each
+    assert choose(65536, 1, 16, SMS) == 103 * 64
+    # uniform 8 x 131,072 tokens, H8: 3 segments of 683 chunks, one wave per pass
+    assert choose(8 * 131072, 8, 8, SMS) == 683 * 64
+    # packed, the same totals: the second pass counted as 8 H s units, so 7
+    # segments of 293 chunks (three waves per pass)
+    assert choose(8 * 131072, 8, 8, SMS, False) == 293 * 64
 
 
 def test_lengths_are_whole_chunks_and_at_least_four(choose):
@@ -57,7 +60,7 @@ def test_invalid_sizes(choose):
         assert choose(*args) == -1
 
 
-def modelled(T, N, H, sms, L):
+def modelled(T, N, H, sms, L, uniform):
     """Chunk-times of the split passes as kda.h documents them (L in chunks,
     None = no split)."""
     chains, n = N * H, -(-(-(-T // N)) // 64)
@@ -65,16 +68,18 @@ def modelled(T, N, H, sms, L):
     if L is None:
         return waves(chains) * (n + 2)
     segs = -(-n // L)
-    return (waves(chains * (segs - 1)) + waves(chains * segs)) * (L + 2) + segs
+    second = segs - 1 if uniform else segs
+    return (waves(chains * (segs - 1)) + waves(chains * second)) * (L + 2) + segs
 
 
+@pytest.mark.parametrize("uniform", [True, False])
 @pytest.mark.parametrize("T,N,H,sms", [(65536, 1, 16, 152), (8 * 131072, 8, 8, 152),
                                        (65536, 1, 16, 76), (3 * 40000, 3, 5, 152),
                                        (1 << 21, 1, 1, 152), (1 << 20, 2, 24, 152)])
-def test_choice_minimises_the_documented_model(choose, T, N, H, sms):
-    L = choose(T, N, H, sms)
-    got = modelled(T, N, H, sms, None if L == -1 else L // 64)
+def test_choice_minimises_the_documented_model(choose, T, N, H, sms, uniform):
+    L = choose(T, N, H, sms, uniform)
+    got = modelled(T, N, H, sms, None if L == -1 else L // 64, uniform)
     n = -(-(-(-T // N)) // 64)
     cap = max(2, 8 * sms // (N * H))  # at most 8 waves of replay units
-    others = [modelled(T, N, H, sms, c) for c in range(4, n) if 2 <= -(-n // c) <= cap]
-    assert got <= min(others + [modelled(T, N, H, sms, None)])
+    others = [modelled(T, N, H, sms, c, uniform) for c in range(4, n) if 2 <= -(-n // c) <= cap]
+    assert got <= min(others + [modelled(T, N, H, sms, None, uniform)])
