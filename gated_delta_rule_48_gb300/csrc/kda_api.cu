@@ -184,20 +184,44 @@ static int64_t auto_segment_tokens(int64_t T, int32_t N, int32_t H, int sm_count
   if (chains >= sms) return -1;
   const int64_t len = ((T + N - 1) / N + kChunk - 1) / kChunk;  // chunks per sequence
   constexpr int64_t kWaveStart = 2, kMinChunks = 4;
+  // A replay that loads its segment's T records from the first pass costs
+  // kTinNum / kTinDen of one that computes them; times below are in
+  // chunk-times x kTinDen.
+  constexpr int64_t kTinNum = 77, kTinDen = 100;
   auto waves = [&](int64_t units) { return (units + sms - 1) / sms; };
-  int64_t best = waves(chains) * (len + kWaveStart), best_L = -1;
+  auto cost = [&](int64_t L) {
+    const int64_t segs = (len + L - 1) / L, last = len - (segs - 1) * L;
+    const int64_t w1 = waves(chains * (segs - 1));
+    const int64_t first = w1 * (L + kWaveStart) * kTinDen;
+    int64_t second;
+    if (uniform) {  // segments 1 .. segs-2 load their records; the last computes its own
+      const int64_t longest = std::max(segs > 2 ? kTinNum * L : 0, kTinDen * last);
+      second = w1 * (longest + kWaveStart * kTinDen);
+    } else {        // lengths unknown here: any segment may be a full-length last one
+      second = waves(chains * segs) * (L + kWaveStart) * kTinDen;
+    }
+    return first + second + segs * kTinDen;
+  };
+  int64_t best = waves(chains) * (len + kWaveStart) * kTinDen, best_L = -1;
   // beyond 8 waves of replay units every extra segment only adds wave starts
   const int64_t s_max = std::min(len / kMinChunks, std::max<int64_t>(2, 8 * sms / chains));
   for (int64_t s = 2; s <= s_max; ++s) {
-    const int64_t L = (len + s - 1) / s;     // chunks per segment
-    const int64_t segs = (len + L - 1) / L;  // segments per sequence at that length
-    if (segs != s) continue;                 // the same cut as a smaller s
-    const int64_t second = uniform ? segs - 1 : segs;
-    const int64_t t =
-        (waves(chains * (segs - 1)) + waves(chains * second)) * (L + kWaveStart) + segs;
-    if (t < best) {
-      best = t;
-      best_L = L;
+    // the lengths that cut a sequence into exactly s segments: (s-1) L < len <= s L
+    const int64_t lo = std::max((len + s - 1) / s, kMinChunks);
+    const int64_t hi = (len + s - 2) / (s - 1) - 1;
+    if (lo > hi) continue;
+    // For fixed s the wave counts are fixed, so the modelled time is piecewise
+    // linear in L: its minimum is at an end of the range or (uniform) where the
+    // loaded segments and the last one take equally long.
+    const int64_t bal = len * kTinDen / ((s - 1) * kTinDen + kTinNum);
+    const int64_t cand[4] = {lo, hi, bal, bal + 1};
+    for (int64_t L : cand) {
+      if (L < lo || L > hi) continue;
+      const int64_t t = cost(L);
+      if (t < best) {
+        best = t;
+        best_L = L;
+      }
     }
   }
   return best_L > 0 ? best_L * kChunk : -1;
@@ -311,7 +335,8 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
                 (long long)capacity64, H);
   const int32_t capacity = static_cast<int32_t>(capacity64);
 
-  // workspace: [segment count | segments | incr_trans | entry_state]
+  // workspace: [segment count | segments | incr_trans | entry_state |
+  //             checkpoint bases | launch orders | T records]
   auto align_up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off_nseg = 0;
   size_t off_segs = align_up(off_nseg + sizeof(int32_t));
@@ -327,7 +352,12 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   size_t off_ord = align_up(off_ck + ck_base_bytes);
   size_t off_ord2 = align_up(off_ord + sizeof(int32_t) * capacity);
   size_t off_nord = align_up(off_ord2 + sizeof(int32_t) * capacity);
-  size_t ws_bytes = align_up(off_nord + 2 * sizeof(int32_t));
+  // T records of the summarised segments (one slot of L / 64 chunks per
+  // segment and head), read back by the second pass
+  const int64_t t_seg_chunks = split ? L / kChunk : 0;
+  size_t off_t = align_up(off_nord + 2 * sizeof(int32_t));
+  size_t t_bytes = split ? static_cast<size_t>(capacity) * H * t_seg_chunks * kTChunkBytes : 0;
+  size_t ws_bytes = align_up(off_t + t_bytes);
 
   // A uniform batch with neither split nor checkpoints needs no plan and no
   // workspace: the chunk kernel takes segment i = sequence i.
@@ -342,9 +372,19 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     e = cudaStreamIsCapturing(s, &cap);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-    e = cap == cudaStreamCaptureStatusNone
-            ? cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), ws_bytes, dev->pool, s)
-            : cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
+    auto alloc = [&](size_t bytes) {
+      return cap == cudaStreamCaptureStatusNone
+                 ? cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), bytes, dev->pool, s)
+                 : cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, s);
+    };
+    e = alloc(ws_bytes);
+    if (e == cudaErrorMemoryAllocation && t_bytes > 0) {
+      // no room for the T records: the second pass recomputes T instead
+      (void)cudaGetLastError();
+      t_bytes = 0;
+      ws_bytes = off_t;
+      e = alloc(ws_bytes);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
   }
 
@@ -369,6 +409,9 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
   a.plan.order2 = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_ord2);
   a.plan.n_order = direct ? nullptr : reinterpret_cast<int32_t*>(ws + off_nord);
   a.plan.first_replayed = split && cu_seqlens == nullptr ? 1 : 0;  // uniform batches
+  a.t_cache = t_bytes > 0 ? reinterpret_cast<unsigned char*>(ws + off_t) : nullptr;
+  a.t_seg_chunks = t_seg_chunks;
+  a.plan.t_records = a.t_cache ? 1 : 0;
   if (direct) a.plan.direct_len = T / N;
   if (want_ckpt) {
     a.plan.ckpt_base = reinterpret_cast<int64_t*>(ws + off_ck);
@@ -388,7 +431,7 @@ static kda_status chunk_fwd_impl(const void* q, const void* k, const void* v,
     if (e == cudaSuccess) e = launch_prefill_pass1(a, s);
     if (e == cudaSuccess) e = launch_segment_scan(a, s);
     a.pass = 2;
-    if (e == cudaSuccess) e = launch_prefill_replay(a, s);
+    if (e == cudaSuccess) e = launch_prefill_pass2(a, s);
   } else if (e == cudaSuccess) {
     e = dump ? launch_prefill_replay_dump(a, s) : launch_prefill_replay(a, s);
   }

@@ -74,7 +74,8 @@ struct Plan {
   // the planner -- segment i is sequence i, direct_len tokens long
   int64_t direct_len = 0;
   // Launch orders written by the planner, each longest first (decreasing
-  // chunk count): order [capacity] for the first pass, order2 [capacity] for
+  // modelled time: the chunk count, scaled for replays that load T records):
+  // order [capacity] for the first pass, order2 [capacity] for
   // the second pass of a split prefill, n_order [2] their lengths; order null:
   // rank = segment id.  Unsplit: order lists every segment.  Split with
   // first_replayed: order = every segment but the last one of a split
@@ -88,6 +89,10 @@ struct Plan {
   // (uniform batches), 0 when it only summarises (every segment but the last)
   // and the second pass replays all segments (packed batches)
   int32_t first_replayed = 0;
+  // the first pass keeps T records for the second (PrefillArgs::t_cache): the
+  // second pass's launch order then counts a summarised segment's chunks at
+  // 0.77 chunk-times each
+  int32_t t_records = 0;
 };
 
 // Problem description shared by the prefill kernels.
@@ -119,7 +124,16 @@ struct PrefillArgs {
   int32_t dump_seg = -1, dump_head = -1;
   int64_t dump_chunk = -1;
   int pass = 1;  // which launch order the kernels walk (2: a split prefill's second pass)
+  // Split prefill: the first pass's summaries store each chunk's T (its tf32
+  // copy, then the bf16 hi and lo halves: kTChunkBytes) at
+  // ((segment * H + head) * t_seg_chunks + chunk) * kTChunkBytes, and the
+  // second pass's replays of those segments load it instead of recomputing
+  // it.  Null: every replay computes its own T.
+  unsigned char* t_cache = nullptr;
+  int64_t t_seg_chunks = 0;  // chunks per segment slot (the split's segment length)
 };
+
+constexpr int64_t kTChunkBytes = 32768;
 
 // Layout of the intermediate dump, in floats: g [64][128], A_kk [64][64],
 // A_qk [64][64], T [64][64], U [64][128], S at the chunk's start [128][128]
@@ -164,10 +178,13 @@ cudaError_t launch_segment_scan(const PrefillArgs& a, cudaStream_t s);
 
 // ---- chunked prefill (kda_prefill_*.cu)
 // tcgen05 kernels (kda_prefill_tc.cu), dk = dv = 128 or 64.  Split prefill:
-// pass 1 replays the first segment of every sequence (from S0) and summarises
-// (B_j, M_j) the middle ones, in one launch; the scan chains the entry states;
-// pass 2 (a.pass = 2) replays segments 1 .. count - 1.  Unsplit: one replay.
+// pass 1 summarises (B_j, M_j) every segment but the last of its sequence,
+// except that uniform batches (plan.first_replayed) replay the first segment
+// from S0 instead, in the same launch; the scan chains the entry states;
+// pass 2 (a.pass = 2) replays the rest, loading the T records of the
+// summarised segments.  Unsplit: one replay.
 cudaError_t launch_prefill_pass1(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_pass2(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_replay(const PrefillArgs& a, cudaStream_t s);
 // the replay with the intermediate dump of a.dump (one chunk of one unit)
 cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s);

@@ -123,10 +123,14 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
   if (s_bad) return;
   const int32_t ns = s_base;
   int32_t* s_count = s_scan;  // reused: [key]
-  auto key_of = [&](int32_t id) {
-    const int64_t len = plan.segs[id].t1 - plan.segs[id].t0;
-    const int64_t chunks = (len + kChunk - 1) / kChunk;
-    return static_cast<int>(chunks < kPlanThreads - 1 ? chunks : kPlanThreads - 1);
+  // sort key: the unit's modelled time in chunk-times (a second-pass replay
+  // that loads its T records takes 0.77 of one per chunk)
+  auto key_of = [&](int32_t id, int list) {
+    const Segment& g = plan.segs[id];
+    const int64_t chunks = (g.t1 - g.t0 + kChunk - 1) / kChunk;
+    const bool loads_t = list == 1 && plan.t_records && g.index + 1 < g.count;
+    const int64_t t = loads_t ? chunks * 77 / 100 : chunks;
+    return static_cast<int>(t < kPlanThreads - 1 ? t : kPlanThreads - 1);
   };
   for (int list = 0; list < 2; ++list) {
     int32_t* out = list ? plan.order2 : plan.order;
@@ -139,7 +143,7 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
     s_count[tid] = 0;
     __syncthreads();
     for (int32_t id = tid; id < ns; id += kPlanThreads)
-      if (kda_guard(id, 1, plan.capacity, err) && in_list(id)) atomicAdd(&s_count[key_of(id)], 1);
+      if (kda_guard(id, 1, plan.capacity, err) && in_list(id)) atomicAdd(&s_count[key_of(id, list)], 1);
     __syncthreads();
     // first rank of key k = number of listed segments with a larger key: an
     // inclusive scan in decreasing key order (thread tid holds key
@@ -162,7 +166,7 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
     __syncthreads();
     for (int32_t id = tid; id < ns; id += kPlanThreads) {
       if (!kda_guard(id, 1, plan.capacity, err) || !in_list(id)) continue;
-      const int32_t rank = atomicAdd(&s_count[key_of(id)], 1);
+      const int32_t rank = atomicAdd(&s_count[key_of(id, list)], 1);
       if (kda_guard(rank, 1, plan.capacity, err)) out[rank] = id;
     }
     __syncthreads();  // s_count is reused by the next list

@@ -111,11 +111,12 @@ constexpr uint32_t kEGl = kG1 + 512;          // e^{g_last} [2][128], by chunk p
 constexpr uint32_t kPC = kEGl + 1024;         // per-channel factors [5][128]: e^{G0}, e^{G1},
                                               // e^{g_last - G0}, e^{g_last - G1}, e^{G1 - G0}
 constexpr uint32_t kBeta = kPC + 5 * 512;
-constexpr uint32_t kBars = kBeta + 256;       // 12 mbarriers, TMEM slot, abort flag
+constexpr uint32_t kBars = kBeta + 256;       // 13 mbarriers, TMEM slot, abort flag
 constexpr uint32_t kSmemBytes = kBars + 128 + 1024;  // + alignment slack
 static_assert(kRXs + 32 * 36 * 4 <= kRAqk, "UT scratch overlaps A_qk");
 static_assert(kTot >= kR + 32768 && kTot + kWarps * 512 <= kR + kRAqk, "scan totals placement");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(13 * 8 + 2 * 4 <= 128, "mbarriers, TMEM slot and abort flag");
 
 struct TcMaps {
   CUtensorMap q, k, v, la;  // la: f32 log alpha, or the bf16 gate logits when fused
@@ -454,7 +455,7 @@ __device__ __forceinline__ bool unit_of(const PrefillArgs& a, int32_t& seg_id, S
 }
 
 // One (segment, head) unit, in summary or replay mode (see the file header).
-template <int MODE, bool FUSED, bool CKPT, bool DUMP>
+template <int MODE, bool FUSED, bool CKPT, bool DUMP, bool TIN = false>
 __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const PrefillArgs& a,
                                                 const int32_t seg_id, const Segment& sg,
                                                 const int h) {
@@ -472,6 +473,11 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
   // only the state-reading products and the state updates are doubled.
   constexpr bool kOut = MODE == kModeReplay;
   constexpr bool kSum = MODE == kModeSummary;
+  // TIN (second pass of a split prefill): a segment that the first pass
+  // summarised (every one but the last of its sequence) takes each chunk's T
+  // from the summary's record instead of the key-row read-out and the UT
+  // transform.  The strip products still run, for A_qk.
+  const bool tin = TIN && kOut && !DUMP && a.t_cache && !last;
   // Width of the caller's tensors: 128, or 64 run zero-padded to 128 (the
   // maps read channels >= 64 as zeros; zero key and query channels add
   // nothing, and zero value channels stay zero, so the 64 x 64 block is
@@ -501,7 +507,8 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
   uint64_t* bar_ready = bars + 6;  // [4] operands of that group ready (one arrive per worker warp)
   uint64_t* bar_raw = bars + 10;   // raw q, k, log_alpha of a chunk read (one arrive per worker warp)
   uint64_t* bar_donep = bars + 11; // replay: P^T = S^T (k e^g)^T committed (issuer 1)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* bar_t = bars + 12;     // TIN replay: the chunk's T record landed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   float* sTot = reinterpret_cast<float*>(sm + kTot);
   float* sG0 = reinterpret_cast<float*>(sm + kG0);
@@ -514,6 +521,12 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
   float* sAkk = reinterpret_cast<float*>(R + kRAkk);
 
   const int64_t n_chunks = (sg.t1 - sg.t0 + C - 1) / C;
+  // T records of this unit: written by the summary, read by a TIN replay
+  const int64_t t_base = (static_cast<int64_t>(seg_id) * H + h) * a.t_seg_chunks;
+  const bool t_ok = (kSum || tin) && a.t_cache && n_chunks <= a.t_seg_chunks &&
+                    kda_guard(t_base, n_chunks,
+                              static_cast<int64_t>(a.plan.capacity) * H * a.t_seg_chunks, a.err);
+  auto t_rec = [&](int64_t m) { return a.t_cache + (t_base + m) * kTChunkBytes; };
   // raw q (replay only), k, and log alpha (f32) or gate logits (bf16)
   const uint32_t qkl_bytes = (kOut ? 32768u : 16384u) + (FUSED ? 16384u : 32768u);
   const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, column quarter
@@ -529,7 +542,12 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
     }
     mbar_init(bar_raw, kWarps);
     mbar_init(bar_donep, 1);
+    mbar_init(bar_t, 1);
     *s_abort = 0;
+    if (tin && !t_ok) {  // no records for this segment (plan and workspace disagree)
+      atomicOr(a.err, kDevErrCapacity);
+      *s_abort = 1;
+    }
     mbar_fence_init();
   }
   if (warp == kWarps) {  // the control warp owns the TMEM allocation
@@ -904,6 +922,8 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
       issue_qkl(sg.t0);
       issue_v(sg.t0);
     }
+    if (tin && who == 0 && n_chunks > 0 && !*s_abort)
+      bulk_prefetch_l2(t_rec(0), static_cast<uint32_t>(kTChunkBytes));
     for (int64_t n = 0; n < n_chunks; ++n) {
       if (who == 1) {  // raw q, k, log_alpha of chunk n read by every worker: stream in n+1
         if (*s_abort) break;
@@ -929,6 +949,18 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
               mma_f16_ss(tmem + cA, kmaj(a0, j, 128 * 128), kmaj(b0, j, 96 * 128), id, j > 0);
           }
           mma_commit(bar_done + 0);
+          // TIN: chunk n's T record into R (the strip A operand) once the
+          // strip MMA has read it; chunk n+1's record on its way into L2
+          if (tin && go) {
+            if (mbar_wait(bar_done + 0, static_cast<uint32_t>(n & 1))) {
+              mbar_arrive_expect_tx(bar_t, static_cast<uint32_t>(kTChunkBytes));
+              bulk_load(R, t_rec(n), static_cast<uint32_t>(kTChunkBytes), bar_t);
+              if (n + 1 < n_chunks)
+                bulk_prefetch_l2(t_rec(n + 1), static_cast<uint32_t>(kTChunkBytes));
+            } else {
+              flag_timeout();
+            }
+          }
         } else {
           if (go) {
             const uint64_t kg = kdesc(KG);
@@ -956,6 +988,10 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
         } else {
           bool ok = go;
           if (ok && !mbar_wait(bar_v, static_cast<uint32_t>(n & 1))) { flag_timeout(); ok = false; }
+          if (tin && ok && !mbar_wait(bar_t, static_cast<uint32_t>(n & 1))) {
+            flag_timeout();
+            ok = false;
+          }
           tc_fence_after();
           if (ok) {
             const uint32_t idu = make_idesc(kFmtBF16, 128, 64, true, false);
@@ -1020,6 +1056,10 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
             }
           } else if (g == 1) {
             if (who == 0) {  // W^T = (k e^g)^T T^T (tf32)
+              if (go && t_ok) {  // T of chunk n kept for the replay of this segment
+                bulk_store(t_rec(n), R, static_cast<uint32_t>(kTChunkBytes));
+                bulk_commit();
+              }
               if (go) {
                 const uint32_t idw = make_idesc(kFmtTF32, 128, 64, false, false);
                 const uint64_t kg = kdesc(KG), tt = kdesc(R + kRT);
@@ -1050,6 +1090,9 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
               else flag_timeout();
             }
           } else if (g == 2) {
+            // the T record has left R before this group commits (the workers
+            // overwrite R once group 2 has completed)
+            if (t_ok && who == 0) bulk_wait_read();
             const uint32_t id = make_idesc(kFmtTF32, 128, 64, false, false);
             if (go && who == 0) {  // U^T -= S^T W^T (KG holds -W)
               const uint64_t wm = kdesc(KG);
@@ -1085,6 +1128,7 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
       }
       if (*s_abort) break;
     }
+    if (kSum && t_ok && who == 0) bulk_wait();  // the T records are written before exit
   };
 
   if (warp >= kWarps) {
@@ -1110,8 +1154,9 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
       const bool dump_chunk = DUMP && dump_unit && n == a.dump_chunk;
       if (dump_chunk) store_state(a.dump, kDumpS, kDumpFloats, 128, kColS, D);  // S at the chunk's start
 
-      // ---- B: strip read-out, UT transform, T to SMEM
-      {
+      // ---- B: strip read-out, UT transform, T to SMEM (TIN: T arrives by
+      //      TMA, and only the query rows are read out)
+      if (!tin || !(quad & 1)) {
         // row L = 32 quad + lane of the strip products: strip s = quad / 2,
         // query rows (A_qk) for even quad, key rows (A_kk) for odd; token r.
         const int s = quad >> 1, is_k = quad & 1;
@@ -1169,6 +1214,24 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
         }
         worker_sync();
       }
+      if (tin) {
+        // once P^T has landed: -P^T rounded to tf32 in TMEM (one 16-column
+        // block per warp) and q e^g into KG (P^T's B operand is consumed)
+        if (warp == 0 && !mbar_wait(bar_donep, static_cast<uint32_t>(n & 1))) flag_timeout();
+        worker_sync();
+        tc_fence_after();
+        {
+          const uint32_t ta = tmem_addr(tmem, 32 * quad, cP + 16 * part);
+          uint32_t pv[16];
+          tmem_ld16(ta, pv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pv[x] = f32_to_tf32_rn(-__uint_as_float(pv[x]));
+          tmem_st16(ta, pv);
+          tmem_wait_st();
+        }
+        write_qeg();
+      } else {
       // The inverse reads only the key rows (odd lane quadrants, A_kk); its
       // first step runs on warps 0 and 1.  Those nine warps meet here; the
       // query-row warps (A_qk) join at the inverse's next barrier, so their
@@ -1194,6 +1257,7 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
         write_qeg();
       }
       if (kP) worker_sync();  // K' and the next scan start after the transform's critical step
+      }
       if (dump_chunk) {  // T (its tf32 operand copy)
         for (int e = tid; e < C * C; e += kWorkers) {
           const int r = e >> 6, i = e & 63;
@@ -1363,6 +1427,19 @@ prefill_pass1_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
     prefill_tc_body<kModeSummary, FUSED, false, false>(maps, a, seg_id, sg, h);
 }
 
+// Second pass of a split prefill: the segments left are replayed from their
+// entry states.  Every one but the last of its sequence was summarised in
+// the first pass, and with the T records kept it loads them (TIN).
+template <bool FUSED, bool CKPT>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_pass2_kernel(const __grid_constant__ TcMaps maps, PrefillArgs a) {
+  int32_t seg_id;
+  Segment sg;
+  int h;
+  if (!unit_of(a, seg_id, sg, h)) return;
+  prefill_tc_body<kModeReplay, FUSED, CKPT, false, true>(maps, a, seg_id, sg, h);
+}
+
 // ---- host side: TMA descriptors
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1401,19 +1478,24 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The kernel a launch runs: one mode, or (PASS1) the mixed first pass.
-template <int MODE, bool FUSED, bool CKPT, bool DUMP, bool PASS1>
+// The kernel a launch runs: one mode (PASS 0), or a split prefill's first
+// (1) or second (2) pass.
+template <int MODE, bool FUSED, bool CKPT, bool DUMP, int PASS>
 struct KernelOf {
   static constexpr auto fn = prefill_tc_kernel<MODE, FUSED, CKPT, DUMP>;
 };
 template <int MODE, bool FUSED, bool CKPT, bool DUMP>
-struct KernelOf<MODE, FUSED, CKPT, DUMP, true> {
+struct KernelOf<MODE, FUSED, CKPT, DUMP, 1> {
   static constexpr auto fn = prefill_pass1_kernel<FUSED, CKPT>;
 };
+template <int MODE, bool FUSED, bool CKPT, bool DUMP>
+struct KernelOf<MODE, FUSED, CKPT, DUMP, 2> {
+  static constexpr auto fn = prefill_pass2_kernel<FUSED, CKPT>;
+};
 
-template <int MODE, bool FUSED, bool CKPT, bool DUMP = false, bool PASS1 = false>
+template <int MODE, bool FUSED, bool CKPT, bool DUMP = false, int PASS = 0>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
-  constexpr auto kern = KernelOf<MODE, FUSED, CKPT, DUMP, PASS1>::fn;
+  constexpr auto kern = KernelOf<MODE, FUSED, CKPT, DUMP, PASS>::fn;
   if (a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   TcMaps maps;
   memset(&maps, 0, sizeof maps);
@@ -1455,10 +1537,18 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t s, const char* name) {
 
 cudaError_t launch_prefill_pass1(const PrefillArgs& a, cudaStream_t s) {
   if (a.ckpt)
-    return a.fused ? launch_tc<kModeReplay, true, true, false, true>(a, s, "kda_prefill_pass1")
-                   : launch_tc<kModeReplay, false, true, false, true>(a, s, "kda_prefill_pass1");
-  return a.fused ? launch_tc<kModeReplay, true, false, false, true>(a, s, "kda_prefill_pass1")
-                 : launch_tc<kModeReplay, false, false, false, true>(a, s, "kda_prefill_pass1");
+    return a.fused ? launch_tc<kModeReplay, true, true, false, 1>(a, s, "kda_prefill_pass1")
+                   : launch_tc<kModeReplay, false, true, false, 1>(a, s, "kda_prefill_pass1");
+  return a.fused ? launch_tc<kModeReplay, true, false, false, 1>(a, s, "kda_prefill_pass1")
+                 : launch_tc<kModeReplay, false, false, false, 1>(a, s, "kda_prefill_pass1");
+}
+
+cudaError_t launch_prefill_pass2(const PrefillArgs& a, cudaStream_t s) {
+  if (a.ckpt)
+    return a.fused ? launch_tc<kModeReplay, true, true, false, 2>(a, s, "kda_prefill_replay")
+                   : launch_tc<kModeReplay, false, true, false, 2>(a, s, "kda_prefill_replay");
+  return a.fused ? launch_tc<kModeReplay, true, false, false, 2>(a, s, "kda_prefill_replay")
+                 : launch_tc<kModeReplay, false, false, false, 2>(a, s, "kda_prefill_replay");
 }
 
 cudaError_t launch_prefill_replay_dump(const PrefillArgs& a, cudaStream_t s) {

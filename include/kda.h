@@ -105,7 +105,9 @@ typedef enum {
  * temporary workspace stream-ordered on `stream` and frees it there: the
  * segment plan (40 bytes per segment) and, when sequences are split,
  * (N + T / segment) * H * dk * (2 dv + dk) * 4 bytes of segment summaries and
- * entry states.
+ * entry states, plus about (N + T / segment) * H * (segment / 64) * 32 KiB
+ * (some 512 bytes per token and head) of T records, which the call leaves out
+ * (recomputing T instead) when the pool cannot provide them.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta,
@@ -170,9 +172,13 @@ kda_status kda_decode_step_t(const kda_tensor *q, const kda_tensor *k,
  * M_j S_in(j) + B_j are scanned, and a second launch replays every segment
  * from its entry state.  In a uniform batch (cu_seqlens NULL) the first launch
  * replays segment 0 from S0 instead of summarising it (its exit state is
- * S_in(1)), so the second replays segments 1 .. last only.  segment_tokens < 0
- * disables splitting.  The result is the same up to rounding; this is the
- * scheduling knob behind the automatic choice.
+ * S_in(1)), so the second replays segments 1 .. last only.  The first launch
+ * also keeps each summarised chunk's UT transform T (32 KiB per chunk and
+ * head, in the call's workspace), and the second launch's replay of that
+ * segment loads it instead of recomputing it, bit for bit the same; if the
+ * workspace pool cannot hold those records, every replay computes its own.
+ * segment_tokens < 0 disables splitting.  The result is the same up to
+ * rounding; this is the scheduling knob behind the automatic choice.
  */
 kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
                                const float *log_alpha, const float *beta,
@@ -188,20 +194,24 @@ kda_status kda_chunk_fwd_split(const void *q, const void *k, const void *v,
  * count (kda_chunk_fwd uses the current device's); uniform is 1 for a uniform
  * batch (cu_seqlens NULL), 0 for a packed one.  Returns a multiple of 64, or
  * -1 for no split.  The choice models each chunk kernel pass as waves of one
- * (segment, head) unit per SM: unsplit, ceil(N H / SMs) waves of the whole
- * sequence; split into s segments per sequence, a first pass of
- * ceil(N H (s - 1) / SMs) waves of one segment and a second of
- * ceil(N H (s - 1) / SMs) waves for a uniform batch (replays of segment 0 and
- * summaries of segments 1 .. s - 2, then replays of segments 1 .. s - 1), of
- * ceil(N H s / SMs) waves for a packed one (summaries of segments 0 .. s - 2,
- * then replays of every segment: shorter segments, which balance the uneven
- * lengths that only the device reads).
+ * (segment, head) unit per SM, a unit of c chunks taking c chunk-times:
+ * unsplit, ceil(N H / SMs) waves of the whole sequence.  Split at L chunks
+ * into s segments per sequence (the last one of l = n - (s - 1) L chunks):
+ *   - uniform batch: a first pass of ceil(N H (s - 1) / SMs) waves of L
+ *     (replays of segment 0, summaries of segments 1 .. s - 2), and a second
+ *     of as many waves of max(0.77 L, l) (replays of segments 1 .. s - 1:
+ *     those that load their T records take 0.77 chunk-times per chunk, the
+ *     last one computes its own; 0.77 L counts only when s > 2);
+ *   - packed batch: ceil(N H (s - 1) / SMs) waves of L, then ceil(N H s / SMs)
+ *     waves of L (summaries of segments 0 .. s - 2, then replays of every
+ *     segment; the lengths, which only the device reads, may make any
+ *     segment a full-length last one).
  * Plus the scan (one chunk-time per segment) and a fixed start of two
- * chunk-times per wave, with sequences taken as total_tokens / n_seqs tokens,
- * segments of at least 4 chunks and at most 8 waves of replay units.  It
- * returns the length with the least modelled time, or -1 when no split beats
- * the unsplit pass (always when N H >= sm_count).  Invalid sizes (any of them
- * <= 0) return -1.
+ * chunk-times per wave, with sequences taken as total_tokens / n_seqs tokens
+ * (n chunks), segments of at least 4 chunks and at most 8 waves of replay
+ * units.  It returns the length with the least modelled time, or -1 when no
+ * split beats the unsplit pass (always when N H >= sm_count).  Invalid sizes
+ * (any of them <= 0) return -1.
  */
 int64_t kda_auto_segment_tokens(int64_t total_tokens, int32_t n_seqs, int32_t n_heads,
                                 int32_t sm_count, int32_t uniform);

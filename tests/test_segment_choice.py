@@ -22,12 +22,14 @@ def test_enough_chains_means_no_split(choose):
 
 
 def test_long_context_shapes(choose):
-    # uniform 1 x 65,536 tokens, H16: 10 segments of 103 chunks -> 144 units in
-    # each pass (16 replays of segment 0 + 128 summaries, then 144 replays),
-    # one wave each
-    assert choose(65536, 1, 16, SMS) == 103 * 64
-    # uniform 8 x 131,072 tokens, H8: 3 segments of 683 chunks, one wave per pass
-    assert choose(8 * 131072, 8, 8, SMS) == 683 * 64
+    # uniform 1 x 65,536 tokens, H16: 10 segments, 144 units in each pass (16
+    # replays of segment 0 + 128 summaries, then 144 replays), one wave each;
+    # 105 chunks leave a 79-chunk last segment, about as long as a 105-chunk
+    # replay that loads its T records (0.77 x 105 = 80.9)
+    assert choose(65536, 1, 16, SMS) == 105 * 64
+    # uniform 8 x 131,072 tokens, H8: 3 segments, one wave per pass; 739
+    # chunks leave a last segment of 570 (0.77 x 739 = 569.0)
+    assert choose(8 * 131072, 8, 8, SMS) == 739 * 64
     # packed, the same totals: the second pass counted as 8 H s units, so 7
     # segments of 293 chunks (three waves per pass)
     assert choose(8 * 131072, 8, 8, SMS, False) == 293 * 64
@@ -61,15 +63,21 @@ def test_invalid_sizes(choose):
 
 
 def modelled(T, N, H, sms, L, uniform):
-    """Chunk-times of the split passes as kda.h documents them (L in chunks,
-    None = no split)."""
+    """Chunk-times x 100 of the split passes as kda.h documents them (L in
+    chunks, None = no split)."""
     chains, n = N * H, -(-(-(-T // N)) // 64)
     waves = lambda u: -(-u // sms)
     if L is None:
-        return waves(chains) * (n + 2)
+        return waves(chains) * (n + 2) * 100
     segs = -(-n // L)
-    second = segs - 1 if uniform else segs
-    return (waves(chains * (segs - 1)) + waves(chains * second)) * (L + 2) + segs
+    last = n - (segs - 1) * L
+    w1 = waves(chains * (segs - 1))
+    first = w1 * (L + 2) * 100
+    if uniform:  # segments 1 .. segs-2 load their T records (0.77 of a chunk-time each)
+        second = w1 * (max(77 * L if segs > 2 else 0, 100 * last) + 200)
+    else:
+        second = waves(chains * segs) * (L + 2) * 100
+    return first + second + segs * 100
 
 
 @pytest.mark.parametrize("uniform", [True, False])
