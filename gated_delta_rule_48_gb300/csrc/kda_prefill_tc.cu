@@ -426,6 +426,17 @@ __device__ __forceinline__ void st_transposed4(unsigned char* tile, int lane, in
   }
 }
 
+// The same four rows without the stagger: at step s every lane writes row
+// 4 lane + s.  Those stores conflict on the shared-memory banks, but the
+// replay's K' measured faster this way than with the selects the stagger needs
+// (the summary, whose K' and k e^g stores sit elsewhere on its chain, did not).
+__device__ __forceinline__ void st_rows4(unsigned char* tile, int lane, int t0,
+                                         const uint4 (&v)[4]) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+    *reinterpret_cast<uint4*>(tile + sw128_offset(D, 4 * lane + s, 4 * t0)) = v[s];
+}
+
 // The (segment, head) unit of this block: one block per unit, rank-major (all
 // heads of launch rank r, then rank r + 1).  The planner's order maps ranks
 // to segments, longest first (the block scheduler hands out blocks in index
@@ -1284,7 +1295,8 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
         uint4 kv[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) kv[x] = pack4_tf32(kp[x]);
-        st_transposed4(KP, lane, r0, kv);
+        if (kOut) st_rows4(KP, lane, r0, kv);
+        else st_transposed4(KP, lane, r0, kv);
       }
       if (kP && n + 1 < n_chunks) scan_chunk(n + 1);  // registers + small tables only
       wait_done_sync(1, n);

@@ -52,6 +52,7 @@ CHILD_TESTS = [
     "tests/test_parity.py::test_lengths_and_head_sizes",
     "tests/test_parity.py::test_varlen_short_and_long_with_empty",
     "tests/test_parity.py::test_segment_split_matches_oracle",
+    "tests/test_parity.py::test_uniform_split_matches_oracle",
     "tests/test_parity.py::test_segment_split_d64_and_no_split_agree",
     "tests/test_parity.py::test_automatic_split_is_the_documented_length",
     "tests/test_parity.py::test_thousands_of_sequences",

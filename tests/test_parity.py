@@ -114,6 +114,17 @@ def test_segment_split_matches_oracle(seg, la):
             segment_tokens=seg)
 
 
+@pytest.mark.parametrize("seg,dk", [(64, 128), (192, 128), (128, 64)])
+def test_uniform_split_matches_oracle(seg, dk):
+    """Forced split of a uniform batch (cu_seqlens NULL): the first pass replays
+    segment 0 of every sequence beside the middle segments' summaries, and the
+    second pass replays the rest, every one but the last from the T records
+    the first pass kept.  777 tokens per sequence end in a ragged chunk."""
+    p = kin.make_prefill([777] * 3, 2, dk, seed=45, s0_std=0.05, log_alpha_fixed=-0.02)
+    assert p.uniform
+    compare(p, segment_tokens=seg)
+
+
 def test_automatic_split_is_the_documented_length():
     """kda_chunk_fwd's automatic split is an explicit split at the length
     kda_auto_segment_tokens reports for this device: the same launches, so
