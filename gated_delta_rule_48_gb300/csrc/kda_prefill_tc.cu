@@ -49,6 +49,15 @@
 // The summary runs C as W^T, U~^T || K', then D (-W to SMEM) and E (U^T -=
 // S^T W^T for both of its states || decay scan of n+1).
 // Raw q, k, log_alpha stream in by TMA one chunk ahead; v after step C.
+//
+// Split prefill: every chunk's T is the same whether the summary or the
+// replay of its segment computes it (the key rows of the strip products do
+// not depend on the query rows).  So the summary keeps each T (tf32 copy and
+// bf16 hi / lo, 32 KiB) in the workspace with one bulk store, and the second
+// pass's replay of a summarised segment (TIN) runs B as: T loaded by one bulk
+// copy into the strip operand's buffer once the strip MMA has read it, only
+// the query rows read out, -P^T rounded on all 16 warps.  Its outputs are
+// bit for bit those of a replay that computes T.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
