@@ -1157,6 +1157,12 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
     __syncwarp();
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kWorkerRegs));
+    // checkpoints: the segment's first token within its sequence, read once
+    // here (a global load at the end of every chunk would sit on the chain);
+    // negative: the unit writes none
+    int32_t ck_seg_off = -1;
+    if (CKPT && kda_guard(sg.first, 1, a.plan.capacity, a.err) && kda_guard(sg.seq, 1, a.N, a.err))
+      ck_seg_off = static_cast<int32_t>(sg.t0 - a.plan.segs[sg.first].t0);
     if (n_chunks > 0) {
       scan_chunk(0);
       worker_sync();
@@ -1358,16 +1364,11 @@ __device__ __forceinline__ void prefill_tc_body(const TcMaps& maps, const Prefil
         signal_ready(0);
       }
       wait_done_sync(3, n);
-      if (CKPT) {  // the state after this chunk, if the sequence has a checkpoint here
+      if (CKPT && ck_seg_off >= 0) {  // the state after this chunk, if the sequence has a checkpoint here
         // tokens of the sequence up to this chunk's end (< 2^31: TMA coordinates are 32-bit)
         const int32_t ci = static_cast<int32_t>(a.plan.ckpt_interval);
-        const bool refs_ok = kda_guard(sg.first, 1, a.plan.capacity, a.err) &&
-                             kda_guard(sg.seq, 1, a.N, a.err);
-        const int32_t pos =
-            refs_ok ? static_cast<int32_t>(sg.t0 - a.plan.segs[sg.first].t0) +
-                          static_cast<int32_t>(n) * C + chunk_valid(n)
-                    : 1;
-        if (refs_ok && pos % ci == 0) {
+        const int32_t pos = ck_seg_off + static_cast<int32_t>(n) * C + chunk_valid(n);
+        if (pos % ci == 0) {
           const int64_t slot = a.plan.ckpt_base[sg.seq] + pos / ci - 1;
           if (slot < a.plan.ckpt_max) {  // 8 columns at a time: few live registers mid-loop
             const int64_t ck_off = (slot * H + h) * DIO * DIO;
