@@ -55,6 +55,7 @@ CHILD_TESTS = [
     "tests/test_parity.py::test_uniform_split_matches_oracle",
     "tests/test_parity.py::test_segment_split_d64_and_no_split_agree",
     "tests/test_parity.py::test_automatic_split_is_the_documented_length",
+    "tests/test_parity.py::test_automatic_uniform_split_is_the_documented_length",
     "tests/test_parity.py::test_thousands_of_sequences",
     "tests/test_parity.py::test_state_aliasing_continuation",
     "tests/test_parity.py::test_decode_steps_equal_prefill_of_same_tokens",

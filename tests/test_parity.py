@@ -145,6 +145,26 @@ def test_automatic_split_is_the_documented_length():
     check_state(auto[1].cpu().numpy(), ref_S)
 
 
+def test_automatic_uniform_split_is_the_documented_length():
+    """The same for a uniform batch (cu_seqlens NULL), where the first pass also
+    replays segment 0 and the second pass loads the T records."""
+    p = kin.make_prefill([4096] * 2, 2, 128, seed=46, s0_std=0.05, log_alpha_fixed=-0.02)
+    assert p.uniform
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = kb.kda_auto_segment_tokens(p.total_T, p.n_seqs, p.H, sms, True)
+    assert L > 0 and -(-4096 // L) >= 3  # 4 chains: several segments, so loaded replays run
+    d = to_device(p)
+    auto = kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], None,
+                            n_seqs=p.n_seqs, segment_tokens=0)
+    expl = kb.kda_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], None,
+                            n_seqs=p.n_seqs, segment_tokens=L)
+    assert kb.kda_get_device_error() == 0
+    assert torch.equal(auto[0], expl[0]) and torch.equal(auto[1], expl[1])
+    ref_o, ref_S = oracle_prefill(p)
+    check_out(auto[0].float().cpu().numpy(), ref_o)
+    check_state(auto[1].cpu().numpy(), ref_S)
+
+
 @pytest.mark.parametrize("seg", [0, 64])
 def test_thousands_of_sequences(seg):
     """2,500 packed sequences of 0..199 tokens: the planner walks them in
