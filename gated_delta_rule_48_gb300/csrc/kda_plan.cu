@@ -178,16 +178,20 @@ plan_kernel(const int32_t* __restrict__ cu, int64_t T, int32_t N, int64_t L, Pla
 // (sequence, head, block of kScanCols state columns), sequential over the
 // sequence's segments.  The whole M_j (D x D f32, from the summary records)
 // is staged in shared memory by cp.async, the next segment's copy in flight
-// while the current one is used; rows are padded by 4 floats so the threads
-// reading 4 different rows hit different banks.
-constexpr int kScanCols = 8;
+// while the current one is used.  The CTA's columns of S_in are kept
+// transposed, so a thread reads 4 consecutive m of its M rows and of its
+// column with one 16-byte load each (the sums still run over m in order);
+// rows are padded by 4 floats so the 4 rows (and 8 columns) a warp reads
+// fall in different banks.
+constexpr int kScanCols = 16;
 constexpr int kScanThreads = 256;
+constexpr int kScanRowStep = kScanThreads / kScanCols;  // a thread's rows: c0 + kScanRowStep r
 
 template <int D>
 struct ScanSmem {
   static constexpr int LD = D + 4;
   float M[2][D * LD];
-  float S[D * kScanCols];
+  float S[kScanCols * LD];  // S_in^T: [column][m]
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -250,30 +254,39 @@ segment_scan_kernel(PrefillArgs a) {
     cp_async_commit();
   };
   stage_M(0, rec_off(s_first + j0));
-  for (int i = tid; i < D * kScanCols; i += kScanThreads) {  // S_in(j0)
+  for (int i = tid; i < D * kScanCols; i += kScanThreads) {  // S_in(j0), transposed
     const int c = i / kScanCols, j = i % kScanCols;
+    float& dst = sm.S[j * LD + c];
     if (j0) {
       const int64_t e = ((static_cast<int64_t>(s_first) + 1) * a.H + h) * static_cast<int64_t>(D) * D +
                         static_cast<int64_t>(c) * D + col0 + j;
-      sm.S[i] = kda_guard(e, 1, n_es, a.err) ? a.entry_state[e] : 0.f;
+      dst = kda_guard(e, 1, n_es, a.err) ? a.entry_state[e] : 0.f;
     } else {
       const int64_t e = ((static_cast<int64_t>(n) * a.H + h) * DIO + c) * DIO + col0 + j;
-      sm.S[i] = (a.S0 && c < DIO && col0 + j < DIO &&
-                 kda_guard(e, 1, static_cast<int64_t>(a.N) * a.H * DIO * DIO, a.err))
-                    ? a.S0[e]
-                    : 0.f;
+      dst = (a.S0 && c < DIO && col0 + j < DIO &&
+             kda_guard(e, 1, static_cast<int64_t>(a.N) * a.H * DIO * DIO, a.err))
+                ? a.S0[e]
+                : 0.f;
     }
   }
-  const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + 32 r
+  const int j = tid % kScanCols, c0 = tid / kScanCols;  // rows c0 + kScanRowStep r
+  // B_j of this thread's outputs, loaded one segment ahead so its latency
+  // overlaps the previous step
+  float b_next[RPT];
+  auto load_B = [&](int64_t seg) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const int64_t e = rec_off(seg) + static_cast<int64_t>(c0 + kScanRowStep * r) * W + col0 + j;
+      b_next[r] = kda_guard(e, 1, n_it, a.err) ? a.incr_trans[e] : 0.f;
+    }
+  };
+  load_B(s_first + j0);
   for (int sgi = j0; sgi + 1 < s_count; ++sgi) {
     const int64_t seg = s_first + sgi;
-    const int64_t roff = rec_off(seg);
     float acc[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {  // B_j
-      const int64_t e = roff + static_cast<int64_t>(c0 + 32 * r) * W + col0 + j;
-      acc[r] = kda_guard(e, 1, n_it, a.err) ? a.incr_trans[e] : 0.f;
-    }
+    for (int r = 0; r < RPT; ++r) acc[r] = b_next[r];  // B_j
+    if (sgi + 2 < s_count) load_B(seg + 1);
     if (sgi + 2 < s_count) {  // stage the next transition while this one is used
       stage_M((sgi - j0 + 1) & 1, rec_off(seg + 1));
       cp_async_wait<1>();
@@ -282,17 +295,24 @@ segment_scan_kernel(PrefillArgs a) {
     }
     __syncthreads();
     const float* Mb = sm.M[(sgi - j0) & 1];
-#pragma unroll 4
-    for (int m = 0; m < D; ++m) {
-      const float sv = sm.S[m * kScanCols + j];
+    const float* Sj = sm.S + j * LD;
+#pragma unroll 2
+    for (int m = 0; m < D; m += 4) {
+      const float4 s4 = *reinterpret_cast<const float4*>(Sj + m);
 #pragma unroll
-      for (int r = 0; r < RPT; ++r) acc[r] = fmaf(Mb[(c0 + 32 * r) * LD + m], sv, acc[r]);
+      for (int r = 0; r < RPT; ++r) {
+        const float4 m4 = *reinterpret_cast<const float4*>(Mb + (c0 + kScanRowStep * r) * LD + m);
+        acc[r] = fmaf(m4.x, s4.x, acc[r]);
+        acc[r] = fmaf(m4.y, s4.y, acc[r]);
+        acc[r] = fmaf(m4.z, s4.z, acc[r]);
+        acc[r] = fmaf(m4.w, s4.w, acc[r]);
+      }
     }
     __syncthreads();  // every thread has read S_in(j) and this M buffer
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
-      const int c = c0 + 32 * r;
-      sm.S[c * kScanCols + j] = acc[r];
+      const int c = c0 + kScanRowStep * r;
+      sm.S[j * LD + c] = acc[r];
       const int64_t e = ((seg + 1) * a.H + h) * static_cast<int64_t>(D) * D +
                         static_cast<int64_t>(c) * D + col0 + j;
       if (kda_guard(e, 1, n_es, a.err)) a.entry_state[e] = acc[r];
